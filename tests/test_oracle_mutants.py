@@ -1,0 +1,52 @@
+"""The pins must catch plausible mistakes: each case below plants one mistake in a
+temporary copy of the oracle source (never in the committed file), rebuilds it, runs
+the pin suite against the copy in a subprocess and expects a failure."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pp_oracle.c")
+
+MUTANTS = {
+    "drop_alpha": ("y[i] = x[i] * r * (double)alpha[i];", "y[i] = x[i] * r;"),
+    "eps_outside_sqrt": ("1.0 / sqrt(ss / (double)n + eps)", "1.0 / (sqrt(ss / (double)n) + eps)"),
+    "rope_sign": ("hv[2 * i] = a * c - b * sn;", "hv[2 * i] = a * c + b * sn;"),
+    "rope_half_split": ("double a = hv[2 * i], b = hv[2 * i + 1];",
+                        "double a = hv[i], b = hv[i + head_dim / 2];"),
+    "window_excludes_current": ("const int n_valid = (int)(p + 1 < W ? p + 1 : W);",
+                                "const int n_valid = (int)(p < W ? (p > 0 ? p : 1) : W);"),
+    "ring_index_no_mod": ("(int64_t)(pos % window) * head_dim", "(int64_t)(pos % (window + 1) % window) * head_dim"),
+    "kv_order_swapped": ("double* k = qkv + d;\n    double* v = qkv + 2 * d;",
+                         "double* v = qkv + d;\n    double* k = qkv + 2 * d;"),
+    "gate_up_swapped": ("h[i] = silu(gu[i]) * gu[F + i];", "h[i] = gu[i] * silu(gu[F + i]);"),
+    "matvec_transposed": ("const uint16_t* wr = w + (int64_t)r * cols;\n    double acc = 0.0;\n    for (int c = 0; c < cols; ++c) acc += ora_bf16_to_f64(wr[c]) * x[c];",
+                          "double acc = 0.0;\n    for (int c = 0; c < cols && c < rows; ++c) acc += ora_bf16_to_f64(w[(int64_t)c * cols + r]) * x[c];"),
+    "attn_no_scale": ("s[j] = dot * scale;", "s[j] = dot;"),
+    "audio_table_off_by_one": ("w->emb_audio + ((int64_t)(r - 1) * (s->audio_card + 1) + column[r]) * d;",
+                               "w->emb_audio + ((int64_t)(r % s->n_q) * (s->audio_card + 1) + column[r]) * d;"),
+    "dep_row_off_by_one": ("int row = k + 1;", "int row = k + (k < 15);"),
+    "dep_no_reset_causal": ("for (int j = 0; j <= k; ++j) {\n          const double* kj",
+                            "for (int j = 0; j <= k && j < 1; ++j) {\n          const double* kj"),
+    "argmax_last_tie": ("if (best < 0 || v[i] > v[best]) best = i;", "if (best < 0 || v[i] >= v[best]) best = i;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor not found: %s" % name
+    shutil.copy(os.path.join(ROOT, "oracle", "pp_oracle.h"), tmp_path / "pp_oracle.h")
+    (tmp_path / "pp_oracle.c").write_text(src.replace(old, new))
+    so = str(tmp_path / "libmutant.so")
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-std=c11", str(tmp_path / "pp_oracle.c"), "-o", so, "-lm"])
+    env = dict(os.environ, PP_ORACLE_SO=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "planted mistake %s was not caught:\n%s" % (name, r.stdout[-2000:])
