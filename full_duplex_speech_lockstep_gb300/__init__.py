@@ -1,0 +1,291 @@
+"""GB300-native lockstep decode tick of the PersonaPlex / Moshi RQ-Transformer.
+
+Thin Python binding of ``libpp.so`` (``include/pp.h``): the functions below have the C
+ABI's names and only marshal arguments; every step of the tick runs in the library's
+CUDA kernels.  PyTorch is used for device memory and streams only.
+
+    import full_duplex_speech_lockstep_gb300 as pp
+    eng = pp.Engine(shape, max_batch, weights)   # weights: dict of device tensors
+    eng.open(0)
+    col = eng.step(prev_column, user_codes)      # int32 [max_batch, 17] device tensor
+
+There is no CPU fallback: if the library is missing or fails to load, this module
+raises.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(HERE, "libpp.so")
+
+ROWS = 17
+PP_OK, PP_EINVAL, PP_E_BUSY, PP_E_RANGE, PP_E_NOTLIVE, PP_E_CUDA, PP_E_NOSPACE = 0, -1, -2, -3, -4, -5, -6
+PP_S_NAN, PP_S_INDEX, PP_S_TIMEOUT = 0x1, 0x2, 0x4
+ERRORS = {PP_EINVAL: "PP_EINVAL", PP_E_BUSY: "PP_E_BUSY", PP_E_RANGE: "PP_E_RANGE",
+          PP_E_NOTLIVE: "PP_E_NOTLIVE", PP_E_CUDA: "PP_E_CUDA", PP_E_NOSPACE: "PP_E_NOSPACE"}
+
+# Order of enum pp_weight in pp.h.
+WEIGHT_NAMES = ["emb_text", "emb_audio", "attn_alpha", "wqkv", "wo", "mlp_alpha", "wgu",
+                "wdown", "out_alpha", "wtext", "dep_inproj", "dep_emb_text", "dep_emb_audio",
+                "dep_attn_alpha", "dep_wqkv", "dep_wo", "dep_mlp_alpha", "dep_wgu",
+                "dep_wdown", "dep_out_alpha", "dep_heads"]
+PP_W_COUNT = len(WEIGHT_NAMES)
+
+# Every function pp.h declares (checked against the header and the library by the tests).
+EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
+           "pp_session_open", "pp_session_close", "pp_session_import", "pp_session_pos",
+           "pp_ring_block", "pp_step", "pp_step_host", "pp_status", "pp_step_kernel_count",
+           "pp_profile_step"]
+
+# enum pp_kernel_kind
+KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
+                "text_head", "depformer", "finish"]
+
+
+class PPError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__("%s failed: %s (%d)" % (fn, ERRORS.get(code, "?"), code))
+        self.code = code
+
+
+class pp_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ["d_model", "n_layers", "n_heads", "ffn", "text_vocab", "audio_card", "n_q",
+                 "dep_d", "dep_layers", "dep_heads", "dep_ffn", "window", "max_batch"]] + [
+        ("eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
+
+
+class pp_weights(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p * PP_W_COUNT)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libpp.so (building it first if it is missing or older than its sources)."""
+    global _lib
+    if _lib is None:
+        from . import build
+        build.build()
+        if not os.path.exists(SO):
+            raise RuntimeError("libpp.so is missing; run __graft_entry__.build()")
+        L = ctypes.CDLL(SO)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.pp_weight_shape.argtypes = [P, I, P, P, P]
+        L.pp_weight_shape.restype = I
+        L.pp_workspace_bytes.argtypes = [P]
+        L.pp_workspace_bytes.restype = ctypes.c_size_t
+        L.pp_create.argtypes = [P, P, P, ctypes.c_size_t, P]
+        L.pp_create.restype = I
+        L.pp_destroy.argtypes = [P]
+        L.pp_destroy.restype = None
+        for f in ["pp_session_open", "pp_session_close"]:
+            getattr(L, f).argtypes = [P, I]
+            getattr(L, f).restype = I
+        L.pp_session_import.argtypes = [P, I, I64]
+        L.pp_session_import.restype = I
+        L.pp_session_pos.argtypes = [P, I, P]
+        L.pp_session_pos.restype = I
+        L.pp_ring_block.argtypes = [P, I, I, I, P]
+        L.pp_ring_block.restype = I
+        L.pp_step.argtypes = [P] * 8
+        L.pp_step.restype = I
+        L.pp_step_host.argtypes = [P] * 8
+        L.pp_step_host.restype = I
+        L.pp_status.argtypes = [P, P, P]
+        L.pp_status.restype = I
+        L.pp_step_kernel_count.argtypes = [P]
+        L.pp_step_kernel_count.restype = I
+        L.pp_profile_step.argtypes = [P] * 10
+        L.pp_profile_step.restype = I
+        _lib = L
+    return _lib
+
+
+def _check(fn, rc):
+    if rc != PP_OK:
+        raise PPError(fn, rc)
+    return rc
+
+
+def make_config(shape, max_batch):
+    """pp_config from an object with the model's dimensions (by attribute name)."""
+    return pp_config(shape.d, shape.n_layers, shape.n_heads, shape.ffn, shape.text_vocab,
+                     shape.audio_card, shape.n_q, shape.dep_d, shape.dep_layers,
+                     shape.dep_heads, shape.dep_ffn, shape.window, int(max_batch),
+                     float(shape.eps), float(shape.rope_base))
+
+
+# ---- the C ABI, one wrapper per entry point -------------------------------------------
+
+def pp_weight_shape(cfg, which):
+    dims = (ctypes.c_int64 * 4)()
+    nd, f32 = ctypes.c_int(), ctypes.c_int()
+    _check("pp_weight_shape", lib().pp_weight_shape(ctypes.byref(cfg), which, dims,
+                                                    ctypes.byref(nd), ctypes.byref(f32)))
+    return tuple(dims[:nd.value]), bool(f32.value)
+
+
+def pp_workspace_bytes(cfg):
+    n = lib().pp_workspace_bytes(ctypes.byref(cfg))
+    if n == 0:
+        raise PPError("pp_workspace_bytes", PP_EINVAL)
+    return n
+
+
+def pp_create(cfg, weight_ptrs, workspace_ptr, ws_bytes):
+    w = pp_weights()
+    for i, p in enumerate(weight_ptrs):
+        w.ptr[i] = p
+    h = ctypes.c_void_p()
+    _check("pp_create", lib().pp_create(ctypes.byref(cfg), ctypes.byref(w), workspace_ptr,
+                                        ws_bytes, ctypes.byref(h)))
+    return h
+
+
+def pp_destroy(h):
+    lib().pp_destroy(h)
+
+
+def pp_session_open(h, slot):
+    return _check("pp_session_open", lib().pp_session_open(h, slot))
+
+
+def pp_session_close(h, slot):
+    return _check("pp_session_close", lib().pp_session_close(h, slot))
+
+
+def pp_session_import(h, slot, pos):
+    return _check("pp_session_import", lib().pp_session_import(h, slot, pos))
+
+
+def pp_session_pos(h, slot):
+    v = ctypes.c_int64()
+    _check("pp_session_pos", lib().pp_session_pos(h, slot, ctypes.byref(v)))
+    return v.value
+
+
+def pp_ring_block(h, layer, slot, kv):
+    p = ctypes.c_void_p()
+    _check("pp_ring_block", lib().pp_ring_block(h, layer, slot, kv, ctypes.byref(p)))
+    return p.value
+
+
+def pp_step(h, prev_column, user_codes, force_mask, forced_tokens, column, logits, stream):
+    return _check("pp_step", lib().pp_step(h, prev_column, user_codes, force_mask,
+                                           forced_tokens, column, logits, stream))
+
+
+def pp_step_host(h, prev_column, user_codes, force_mask, forced_tokens, column, logits, stream):
+    return _check("pp_step_host", lib().pp_step_host(h, prev_column, user_codes, force_mask,
+                                                     forced_tokens, column, logits, stream))
+
+
+def pp_status(h, stream):
+    v = ctypes.c_uint32()
+    _check("pp_status", lib().pp_status(h, stream, ctypes.byref(v)))
+    return v.value
+
+
+def pp_step_kernel_count(h):
+    return lib().pp_step_kernel_count(h)
+
+
+def pp_profile_step(h, prev_column, user_codes, force_mask, forced_tokens, column, logits,
+                    stream, kind_ms, kind_launches):
+    """kind_ms: ctypes double array, kind_launches: ctypes int64 array (accumulated)."""
+    return _check("pp_profile_step", lib().pp_profile_step(
+        h, prev_column, user_codes, force_mask, forced_tokens, column, logits, stream,
+        kind_ms, kind_launches))
+
+
+# ---- convenience wrapper over torch device memory ---------------------------------------
+
+class Engine:
+    """One engine over torch-owned device memory (weights dict + workspace)."""
+
+    def __init__(self, shape, max_batch, weights, device="cuda"):
+        import torch
+        self.torch = torch
+        self.shape = shape
+        self.B = int(max_batch)
+        self.cfg = make_config(shape, max_batch)
+        self.weights = weights
+        ptrs = []
+        for i, name in enumerate(WEIGHT_NAMES):
+            t = weights[name]
+            dims, f32 = pp_weight_shape(self.cfg, i)
+            if tuple(t.shape) != dims or t.element_size() != (4 if f32 else 2):
+                raise ValueError("weight %s: shape %s, expected %s" % (name, tuple(t.shape), dims))
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weight %s must be a contiguous CUDA tensor" % name)
+            ptrs.append(t.data_ptr())
+        self.ws_bytes = pp_workspace_bytes(self.cfg)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.h = pp_create(self.cfg, ptrs, self.workspace.data_ptr(), self.ws_bytes)
+        self.logits_ld = shape.text_vocab + shape.n_q * shape.audio_card
+        self.column = torch.empty((self.B, ROWS), dtype=torch.int32, device=device)
+
+    def close_engine(self):
+        if self.h:
+            pp_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close_engine()
+        except Exception:
+            pass
+
+    def _stream(self):
+        return self.torch.cuda.current_stream().cuda_stream
+
+    def open(self, slot):
+        pp_session_open(self.h, slot)
+
+    def close(self, slot):
+        pp_session_close(self.h, slot)
+
+    def import_session(self, slot, pos):
+        pp_session_import(self.h, slot, pos)
+
+    def pos(self, slot):
+        return pp_session_pos(self.h, slot)
+
+    def ring_block(self, layer, slot, kv):
+        return pp_ring_block(self.h, layer, slot, kv)
+
+    def kernel_count(self):
+        return pp_step_kernel_count(self.h)
+
+    def status(self):
+        return pp_status(self.h, self._stream())
+
+    def step(self, prev_column, user_codes, force_mask=None, forced=None, logits=None,
+             out=None):
+        """One tick on device tensors; returns the column tensor (``out`` or the
+        engine's own buffer, overwritten by the next step)."""
+        col = self.column if out is None else out
+        pp_step(self.h, prev_column.data_ptr(), user_codes.data_ptr(),
+                None if force_mask is None else force_mask.data_ptr(),
+                None if forced is None else forced.data_ptr(), col.data_ptr(),
+                None if logits is None else logits.data_ptr(), self._stream())
+        return col
+
+    def profile_step(self, prev_column, user_codes, kind_ms, kind_launches, out=None):
+        """One tick through the profiling graph; accumulates per-kind ms / launches."""
+        col = self.column if out is None else out
+        pp_profile_step(self.h, prev_column.data_ptr(), user_codes.data_ptr(), None, None,
+                        col.data_ptr(), None, self._stream(), kind_ms, kind_launches)
+        return col
+
+    def step_host(self, prev_column, user_codes, force_mask, forced, column, logits=None):
+        """One tick on host (numpy or pinned torch) buffers; blocks until done."""
+        def ptr(a):
+            if a is None:
+                return None
+            return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+        pp_step_host(self.h, ptr(prev_column), ptr(user_codes), ptr(force_mask), ptr(forced),
+                     ptr(column), ptr(logits), self._stream())
+        return column

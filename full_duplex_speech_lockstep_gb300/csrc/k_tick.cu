@@ -1,0 +1,364 @@
+// k_tick.cu - the light kernels of one lockstep tick: control + 17-table embedding
+// sum + RoPE angle table, RMSNorm, RoPE + ring-KV write, the fused greedy heads, the
+// depformer step attention and the end-of-tick bookkeeping.
+#include <math.h>
+
+#include "pp_internal.cuh"
+
+namespace pp {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  // round to nearest even, NaN kept quiet
+  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
+  a = (a & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : a + 0x7FFFu + ((a >> 16) & 1u);
+  b = (b & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : b + 0x7FFFu + ((b >> 16) & 1u);
+  return (a >> 16) | (b & 0xFFFF0000u);
+}
+
+// Fixed-order block sum: per-warp butterfly, then warp 0 adds the warp totals in order.
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* sh) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < NT / 32; ++w) t += sh[w];
+    sh[NT / 32] = t;
+  }
+  __syncthreads();
+  float r = sh[NT / 32];
+  __syncthreads();
+  return r;
+}
+
+}  // namespace
+
+// ---- control, embedding, RoPE table --------------------------------------------------
+// One CTA per slot.  Applies the host's control word (open/close/reset position),
+// validates the previous column, sums its 17 embedding rows in fp32 in row order
+// (text row first), and tabulates cos/sin of this frame's RoPE angles from fp64.
+__global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
+  const int s = blockIdx.x;
+  __shared__ int col[kRows];
+  __shared__ int live_s, pos_s;
+  if (threadIdx.x == 0) {
+    const int c = b.ctl[s];
+    if (c & 2) {             // (re)open: set the position once, then clear the request
+      b.pos[s] = b.ctl_pos[s];
+      b.ctl[s] = c & 1;
+    }
+    b.live[s] = c & 1;
+    live_s = c & 1;
+    pos_s = b.pos[s];
+  }
+  __syncthreads();
+  if (threadIdx.x < kRows) {
+    const int r = threadIdx.x;
+    const int lim = (r == 0) ? D.Vt : D.Va;   // the initial token is the last table row
+    int v = b.in_col[s * kRows + r];
+    if (v < 0 || v > lim) {
+      if (live_s) atomicOr(b.status, PP_S_INDEX);
+      v = lim;
+    }
+    col[r] = v;
+  }
+  __syncthreads();
+  float* x = b.x + (size_t)s * D.d;
+  for (int i = threadIdx.x * 8; i < D.d; i += blockDim.x * 8) {
+    float acc[8];
+    if (!live_s) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+    } else {
+      float e[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(b.emb_text + (size_t)col[0] * D.d + i)), acc);
+      for (int r = 1; r < kRows; ++r) {
+        const uint16_t* row = b.emb_audio + ((size_t)(r - 1) * (D.Va + 1) + col[r]) * D.d + i;
+        unpack8(__ldg(reinterpret_cast<const uint4*>(row)), e);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc[t] += e[t];
+      }
+    }
+    reinterpret_cast<float4*>(x + i)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(x + i)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  // RoPE angles pos * base^(-2i/Dh), evaluated in fp64 and rounded once to fp32
+  for (int i = threadIdx.x; i < D.Dh / 2; i += blockDim.x) {
+    const double theta =
+        (double)pos_s * pow((double)D.rope_base, -2.0 * (double)i / (double)D.Dh);
+    double sn, cs;
+    sincos(theta, &sn, &cs);
+    b.rope_cs[((size_t)s * (D.Dh / 2) + i) * 2] = (float)cs;
+    b.rope_cs[((size_t)s * (D.Dh / 2) + i) * 2 + 1] = (float)sn;
+  }
+}
+
+cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s) {
+  k_begin<<<D.B, 256, 0, s>>>(D, b);
+  return cudaGetLastError();
+}
+
+// ---- RMSNorm ---------------------------------------------------------------------------
+// out[b, i] = x[b, i] / sqrt(mean_j x[b, j]^2 + eps) * alpha[i], one CTA per slot; the
+// sum of squares is taken in a fixed order that does not depend on the batch size.
+__global__ void __launch_bounds__(512) k_rmsnorm(const float* __restrict__ x, int ldx,
+                                                 const float* __restrict__ alpha, int K,
+                                                 float eps, float* __restrict__ out, int ldo,
+                                                 uint16_t* __restrict__ op, int Bp) {
+  __shared__ float sh[17];
+  const int b = blockIdx.x;
+  const float* xr = x + (size_t)b * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < K; i += 512) ss = fmaf(xr[i], xr[i], ss);
+  ss = block_sum<512>(ss, sh);
+  const float r = 1.0f / sqrtf(ss / (float)K + eps);
+  for (int i = threadIdx.x; i < K; i += 512) {
+    const float v = xr[i] * r * alpha[i];
+    if (out) out[(size_t)b * ldo + i] = v;
+    if (op) op_store(op, K, Bp, b, i, v);
+  }
+}
+
+cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
+                           float* out, int ldo, uint16_t* op, cudaStream_t s) {
+  k_rmsnorm<<<D.B, 512, 0, s>>>(x, ldx, alpha, K, D.eps, out, ldo, op, D.Bp);
+  return cudaGetLastError();
+}
+
+// ---- RoPE + ring write -----------------------------------------------------------------
+// One CTA per (slot, head), one thread per rotation pair.  q is rotated and pre-scaled
+// by log2(e)/sqrt(Dh) (the attention kernel works in base 2); k is rotated; k and v are
+// rounded to bf16 into ring index pos mod W of this layer's ring.
+__global__ void k_rope_ring(Dims D, Buffers b, int layer) {
+  const int s = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+  if (!b.live[s] || i >= D.Dh / 2) return;
+  const int p = b.pos[s];
+  const int widx = p % D.W;
+  const float c = b.rope_cs[((size_t)s * (D.Dh / 2) + i) * 2];
+  const float sn = b.rope_cs[((size_t)s * (D.Dh / 2) + i) * 2 + 1];
+  const float* row = b.qkv + (size_t)s * 3 * D.d + h * D.Dh + 2 * i;
+  const float q0 = row[0], q1 = row[1];
+  const float k0 = row[D.d], k1 = row[D.d + 1];
+  const float v0 = row[2 * D.d], v1 = row[2 * D.d + 1];
+  const float qs = 1.4426950408889634f / sqrtf((float)D.Dh);
+  float* q = b.q + (size_t)s * D.d + h * D.Dh + 2 * i;
+  q[0] = (q0 * c - q1 * sn) * qs;
+  q[1] = (q0 * sn + q1 * c) * qs;
+  const float kr0 = k0 * c - k1 * sn, kr1 = k0 * sn + k1 * c;
+  const size_t blk = (size_t)D.W * D.Dh;
+  const size_t kbase = ((((size_t)layer * D.B + s) * 2 + 0) * D.H + h) * blk;
+  const size_t vbase = ((((size_t)layer * D.B + s) * 2 + 1) * D.H + h) * blk;
+  const size_t off = (size_t)widx * D.Dh + 2 * i;
+  *reinterpret_cast<uint32_t*>(b.ring + kbase + off) = pack_bf16x2(kr0, kr1);
+  *reinterpret_cast<uint32_t*>(b.ring + vbase + off) = pack_bf16x2(v0, v1);
+}
+
+cudaError_t launch_rope_ring(const Dims& D, const Buffers& b, int layer, cudaStream_t s) {
+  k_rope_ring<<<dim3(D.B, D.H), (D.Dh / 2 + 31) / 32 * 32, 0, s>>>(D, b, layer);
+  return cudaGetLastError();
+}
+
+// ---- greedy heads ----------------------------------------------------------------------
+// Argmax over fp32 logits: the lowest index holding the maximum; NaN is never chosen
+// and raises PP_S_NAN.  The comparison is order independent, so any reduction tree
+// gives the same index.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__device__ int block_argmax(const float* __restrict__ lg, int n, uint32_t* status) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  __shared__ int nan_seen;
+  if (threadIdx.x == 0) nan_seen = 0;
+  __syncthreads();
+  float bv = -INFINITY;
+  int bi = 0x7FFFFFFF;
+  bool nan = false;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float v = lg[i];
+    if (isnan(v)) { nan = true; continue; }
+    if (better(v, i, bv, bi)) { bv = v; bi = i; }
+  }
+  if (nan) nan_seen = 1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+      if (better(sv[w], si[w], sv[0], si[0])) { sv[0] = sv[w]; si[0] = si[w]; }
+    if (nan_seen) atomicOr(status, PP_S_NAN);
+    if (si[0] == 0x7FFFFFFF) si[0] = 0;
+  }
+  __syncthreads();
+  const int r = si[0];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) k_text_argmax(Dims D, Buffers b) {
+  const int s = blockIdx.x;
+  if (!b.live[s]) {
+    if (threadIdx.x == 0) { b.out_col[s * kRows] = -1; b.tok[s] = 0; }
+    return;
+  }
+  const int am = block_argmax(b.logits + (size_t)s * D.logits_ld, D.Vt, b.status);
+  if (threadIdx.x == 0) {
+    int t = am;
+    if (b.in_fmask[s * kRows]) {
+      t = b.in_forced[s * kRows];
+      if (t < 0 || t > D.Vt) { atomicOr(b.status, PP_S_INDEX); t = D.Vt; }
+    }
+    b.out_col[s * kRows] = t;
+    b.tok[s] = t;
+  }
+}
+
+cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s) {
+  k_text_argmax<<<D.B, 1024, 0, s>>>(D, b);
+  return cudaGetLastError();
+}
+
+// Step k of the depformer decides row k+1: agent rows 1..8 are greedy unless forced,
+// user rows 9..16 take this frame's user codes.
+__global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step) {
+  const int s = blockIdx.x, row = step + 1;
+  if (!b.live[s]) {
+    if (threadIdx.x == 0) { b.out_col[s * kRows + row] = -1; b.tok[s] = 0; }
+    return;
+  }
+  int t = 0;
+  if (row <= PP_AGENT_ROWS && !b.in_fmask[s * kRows + row])
+    t = block_argmax(b.logits + (size_t)s * D.logits_ld + D.Vt + (size_t)step * D.Va, D.Va,
+                     b.status);
+  if (threadIdx.x == 0) {
+    if (row <= PP_AGENT_ROWS) {
+      if (b.in_fmask[s * kRows + row]) t = b.in_forced[s * kRows + row];
+    } else {
+      t = b.in_user[s * PP_USER_ROWS + row - 1 - PP_AGENT_ROWS];
+    }
+    if (t < 0 || t > D.Va) { atomicOr(b.status, PP_S_INDEX); t = D.Va; }
+    b.out_col[s * kRows + row] = t;
+    b.tok[s] = t;
+  }
+}
+
+cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s) {
+  k_dep_argmax<<<D.B, 1024, 0, s>>>(D, b, step);
+  return cudaGetLastError();
+}
+
+// ---- depformer step attention ------------------------------------------------------------
+// One CTA per slot, one warp per head.  Appends this step's k, v (fp32) to the frame's
+// cache and attends causally over steps 0..step (no positional encoding); the cache is
+// indexed by step, so a new frame overwrites it from step 0 (reset each frame).
+template <int E>  // head dim / 32
+__global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
+  const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (h >= D.Hd) return;
+  float* out = b.dout + (size_t)s * D.dd + h * D.Dhd;
+  if (!b.live[s]) {
+    for (int e = 0; e < E; ++e) {
+      out[lane + 32 * e] = 0.f;
+      if (op) op_store(b.op_do, D.dd, D.Bp, s, h * D.Dhd + lane + 32 * e, 0.f);
+    }
+    return;
+  }
+  const float* row = b.dqkv + (size_t)s * 3 * D.dd + h * D.Dhd;
+  float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
+  float q[E], kk[E], vv[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    q[e] = row[lane + 32 * e];
+    kk[e] = row[D.dd + lane + 32 * e];
+    vv[e] = row[2 * D.dd + lane + 32 * e];
+    cache[(size_t)step * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kk[e];
+    cache[(size_t)step * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] = vv[e];
+  }
+  const float scale = 1.0f / sqrtf((float)D.Dhd);
+  float sc[16];
+  float m = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    if (t > step) break;
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float kv = (t == step) ? kk[e] : cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
+      dot = fmaf(q[e], kv, dot);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    sc[t] = dot * scale;
+    m = fmaxf(m, sc[t]);
+  }
+  float l = 0.f, acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    if (t > step) break;
+    const float p = expf(sc[t] - m);
+    l += p;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float vx = (t == step) ? vv[e] : cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
+      acc[e] = fmaf(p, vx, acc[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float v = acc[e] / l;
+    out[lane + 32 * e] = v;
+    if (op) op_store(b.op_do, D.dd, D.Bp, s, h * D.Dhd + lane + 32 * e, v);
+  }
+}
+
+cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
+                            cudaStream_t s) {
+  const int threads = D.Hd * 32;
+  switch (D.Dhd) {
+    case 32: k_dep_attn<1><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
+    case 64: k_dep_attn<2><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
+    case 128: k_dep_attn<4><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---- end of tick -----------------------------------------------------------------------
+__global__ void k_finish(Dims D, Buffers b) {
+  const int s = blockIdx.x, r = threadIdx.x;
+  if (!b.live[s]) {
+    if (r < kRows) b.out_col[s * kRows + r] = -1;
+    return;
+  }
+  if (r == 0) b.pos[s] += 1;
+}
+
+cudaError_t launch_finish(const Dims& D, const Buffers& b, cudaStream_t s) {
+  k_finish<<<D.B, 32, 0, s>>>(D, b);
+  return cudaGetLastError();
+}
+
+}  // namespace pp

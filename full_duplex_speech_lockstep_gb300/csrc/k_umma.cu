@@ -1,0 +1,384 @@
+// k_umma.cu - the tick's weight contractions on the 5th-generation tensor cores.
+//
+//   Y[b, m] (op)= sum_k W[m, k] x[b, k]      for every slot b and output row m
+//
+// Swap-AB: the bf16 weight matrix is the MMA's A operand (M = 128 output rows per
+// tile), the batch is its N dimension.  Activations are fed as two bf16 rows per slot,
+// hi = bf16(x) and lo = bf16(x - hi), so that x is carried to ~16 significant bits and
+// the result equals an fp32-activation product to within fp32 accumulation rounding;
+// the epilogue adds the hi and lo accumulator columns.  The contraction streams each
+// weight byte once, so the extra N columns cost tensor-core time only, which a
+// weight-streaming kernel has to spare.
+//
+// One CTA = one (M-tile, K-split) unit, 4 warps, two CTAs per SM:
+//   warp 0 lane 0  TMA producer: weight tile (two 64-row boxes) + activation tile per
+//                  64-wide k-block into a ring of shared-memory stages (128B swizzle);
+//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per k-block into a TMEM
+//                  accumulator [128 lanes x N columns], tcgen05.commit frees the stage;
+//   all 4 warps    epilogue: tcgen05.ld of their 32 TMEM lanes, hi + lo, then either
+//                  the final epilogue (one split) or an fp32 partial; the last CTA of
+//                  an M-tile (atomic ticket) adds the partials in split order and runs
+//                  the final epilogue.  The split count depends only on the matrix
+//                  shape and the SM count, never on the batch, so a session's bits do
+//                  not depend on the other sessions.
+// Every mbarrier wait is bounded; on expiry the kernel raises PP_S_TIMEOUT, drains
+// its own copies (bounded), frees its TMEM and returns.
+#include <cuda.h>
+#include <math.h>
+
+#include "pp_internal.cuh"
+
+namespace pp {
+
+namespace {
+
+constexpr int kBK = 64;              // k elements per block (128 bytes of bf16)
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P1;\n mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, P1;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false after kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile, 128-byte swizzle, 8-row atoms of
+// 1024 bytes stacked along M/N (stride 1024), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator.
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+template <int N>
+struct Cfg {
+  static constexpr int kABytes = 128 * kBK * 2;          // 16 KB weight tile
+  static constexpr int kBBytes = N * kBK * 2;            // activation tile
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (96 * 1024) / kStageBytes < 8 ? (96 * 1024) / kStageBytes : 8;
+  static constexpr int kTmemCols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <int N>
+__global__ void __launch_bounds__(128, 2)
+    k_umma(const UmmaArgs a, const __grid_constant__ CUtensorMap mapA,
+           const __grid_constant__ CUtensorMap mapB) {
+  using C = Cfg<N>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars[0..S) full, bars[S..2S) empty, bars[2S] done; then the TMEM address and flags
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
+  const int kb0 = (int)(((long long)sp * a.kblocks) / a.splits);
+  const int kb1 = (int)(((long long)(sp + 1) * a.kblocks) / a.splits);
+  const int nkb = kb1 - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&bars[s]), 1);
+      mbar_init(smem_u32(&bars[C::kStages + s]), 1);
+    }
+    mbar_init(smem_u32(&bars[2 * C::kStages]), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  // rows of the two 64-row weight boxes of this tile
+  int rowA0, rowA1;
+  if (a.pair_rows) {            // gate rows then the matching up rows
+    rowA0 = a.row0 + mt * 64;
+    rowA1 = a.row0 + a.pair_rows + mt * 64;
+  } else {
+    rowA0 = a.row0 + mt * 128;
+    rowA1 = rowA0 + 64;
+  }
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer ------------------------------------------------------------------
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % C::kStages;
+      if (i >= C::kStages &&
+          !mbar_wait(smem_u32(&bars[C::kStages + s]), ((i / C::kStages) - 1) & 1)) {
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      uint8_t* sa = smem + s * C::kStageBytes;
+      uint8_t* sb = sa + C::kABytes;
+      const uint32_t full = smem_u32(&bars[s]);
+      mbar_expect_tx(full, C::kStageBytes);
+      const int kx = (kb0 + i) * kBK;
+      tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
+      tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+      tma_load_2d(smem_u32(sb), &mapB, kx, 0, full);
+      ++issued;
+    }
+    if (*abort_flag) {  // drain this CTA's copies still in flight (bounded)
+      for (int i = 0; i < issued; ++i) mbar_wait(smem_u32(&bars[i % C::kStages]), (i / C::kStages) & 1);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer --------------------------------------------------------------------
+    constexpr uint32_t idesc = instr_desc(128, N);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % C::kStages;
+      if (!mbar_wait(smem_u32(&bars[s]), (i / C::kStages) & 1)) {
+        *abort_flag = 1;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t sa = smem_u32(smem + s * C::kStageBytes);
+      const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        umma_bf16(tmem, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), idesc,
+                  (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(smem_u32(&bars[C::kStages + s]));
+    }
+    umma_commit(smem_u32(&bars[2 * C::kStages]));
+  }
+  __syncwarp();
+
+  // ---- epilogue ----------------------------------------------------------------------
+  const bool done = mbar_wait(smem_u32(&bars[2 * C::kStages]), 0);
+  if (!done) *abort_flag = 1;
+  __syncthreads();
+  const bool ok = !*abort_flag && nkb > 0;
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+  const int r = warp * 32 + lane;            // TMEM lane = tile row
+  const int B = a.B, Bp = N / 2;
+  // output row of this thread
+  int m;
+  if (a.pair_rows) m = mt * 64 + (r & 63);   // gate (r < 64) or up (r >= 64) of row m
+  else m = mt * 128 + r;
+  const bool row_ok = a.pair_rows ? (m < a.pair_rows) : (m < a.M);
+
+  float acc[N / 2];
+#pragma unroll
+  for (int c = 0; c < N / 2; c += 8) {
+    float hi[8], lo[8];
+    const uint32_t t = tmem + ((uint32_t)(warp * 32) << 16);
+    if (ok) {
+      tmem_ld8(t + c, hi);
+      tmem_ld8(t + Bp + c, lo);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) hi[j] = lo[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[c + j] = hi[j] + lo[j];
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(C::kTmemCols));
+  if (!ok) {
+    if (threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
+    return;
+  }
+
+  // split-K: partial [split][b][tile row] then the last CTA of the tile reduces in order
+  if (a.splits > 1) {
+    float* part = a.partial + (size_t)mt * a.splits * B * 128;
+#pragma unroll
+    for (int b = 0; b < N / 2; ++b)
+      if (b < B) part[((size_t)sp * B + b) * 128 + r] = acc[b];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned prev = atomicAdd(a.counter + mt, 1u);
+      *last_flag = (prev == (unsigned)(a.splits - 1));
+    }
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+#pragma unroll
+    for (int b = 0; b < N / 2; ++b) acc[b] = 0.f;
+    for (int s = 0; s < a.splits; ++s) {
+#pragma unroll
+      for (int b = 0; b < N / 2; ++b)
+        if (b < B) acc[b] += __ldcg(part + ((size_t)s * B + b) * 128 + r);
+    }
+    if (threadIdx.x == 0) a.counter[mt] = 0u;
+  }
+
+  // ---- final epilogue ------------------------------------------------------------------
+  if (a.epi == EPI_SILU) {
+    float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
+    if (r >= 64)
+      for (int b = 0; b < B; ++b) xch[(r - 64) * Bp + b] = acc[b];
+    __syncthreads();
+    if (r < 64 && row_ok) {
+#pragma unroll
+      for (int b = 0; b < N / 2; ++b) {
+        if (b < B) {
+          const float g = acc[b], u = xch[r * Bp + b];
+          op_store(a.op_out, a.ld_op, a.Bp_out, b, m, g / (1.0f + expf(-g)) * u);
+        }
+      }
+    }
+    return;
+  }
+  if (!row_ok) return;
+#pragma unroll
+  for (int b = 0; b < N / 2; ++b) {
+    if (b >= B) continue;
+    float v = acc[b];
+    float* y = a.Y + (size_t)b * a.ldy + m;
+    if (a.epi == EPI_STORE) {
+      *y = v;
+    } else if (a.epi == EPI_ADD) {
+      v += *y;
+      *y = v;
+    } else {  // EPI_EMB
+      v += bf16_to_f32(a.emb[(size_t)a.tok[b] * a.M + m]);
+      *y = v;
+    }
+  }
+}
+
+}  // namespace
+
+template <int N>
+static cudaError_t umma_n(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
+                          cudaStream_t s) {
+  const int grid = a.m_tiles * a.splits;
+  k_umma<N><<<grid, 128, Cfg<N>::kSmem, s>>>(a, mA, mB);
+  return cudaGetLastError();
+}
+
+template <int N>
+static cudaError_t setup_n() {
+  return cudaFuncSetAttribute(k_umma<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<N>::kSmem);
+}
+
+// Raise the dynamic shared-memory limit of the kernel for N (call before capture).
+cudaError_t umma_setup(int N) {
+  switch (N) {
+    case 16: return setup_n<16>();
+    case 32: return setup_n<32>();
+    case 48: return setup_n<48>();
+    case 64: return setup_n<64>();
+    case 80: return setup_n<80>();
+    case 96: return setup_n<96>();
+    case 112: return setup_n<112>();
+    case 128: return setup_n<128>();
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
+                        cudaStream_t s) {
+  switch (a.N) {
+    case 16: return umma_n<16>(a, mA, mB, s);
+    case 32: return umma_n<32>(a, mA, mB, s);
+    case 48: return umma_n<48>(a, mA, mB, s);
+    case 64: return umma_n<64>(a, mA, mB, s);
+    case 80: return umma_n<80>(a, mA, mB, s);
+    case 96: return umma_n<96>(a, mA, mB, s);
+    case 112: return umma_n<112>(a, mA, mB, s);
+    case 128: return umma_n<128>(a, mA, mB, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int umma_stage_count(int n) {
+  switch (n) {
+    case 16: return Cfg<16>::kStages;
+    case 32: return Cfg<32>::kStages;
+    case 48: return Cfg<48>::kStages;
+    case 64: return Cfg<64>::kStages;
+    case 80: return Cfg<80>::kStages;
+    case 96: return Cfg<96>::kStages;
+    case 112: return Cfg<112>::kStages;
+    case 128: return Cfg<128>::kStages;
+    default: return 0;
+  }
+}
+
+}  // namespace pp

@@ -1,0 +1,525 @@
+// pp_api.cu - the C ABI (include/pp.h): engine creation over caller-owned weights and
+// workspace, the session table, and one lockstep tick captured as a CUDA graph.
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "pp_internal.cuh"
+
+using namespace pp;
+
+// Timing events recorded at every kernel boundary of the profiling graph.
+struct Prof {
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kind;           // kind of the kernel that starts at ev[i]
+  cudaError_t mark(int k, cudaStream_t s) {
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) return err;
+    ev.push_back(e);
+    kind.push_back(k);
+    return cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  }
+  void clear() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    ev.clear();
+    kind.clear();
+  }
+};
+
+struct pp_engine {
+  pp_config cfg;
+  Dims D;
+  Buffers buf;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int n_kernels = 0;
+  cudaGraph_t prof_graph = nullptr;
+  cudaGraphExec_t prof_exec = nullptr;
+  Prof prof;
+  std::vector<int32_t> ctl, ctl_pos;   // uploaded before the next tick when dirty
+  bool ctl_dirty = false;
+  std::vector<int64_t> pos;            // host mirror of each open slot's position
+  std::vector<uint8_t> open;
+};
+
+namespace {
+
+bool head_dim_ok(int hd) { return hd == 32 || hd == 64 || hd == 128; }
+
+bool config_ok(const pp_config* c) {
+  if (!c) return false;
+  if (c->d_model <= 0 || c->n_layers <= 0 || c->n_heads <= 0 || c->ffn <= 0) return false;
+  if (c->d_model % c->n_heads || !head_dim_ok(c->d_model / c->n_heads)) return false;
+  if (c->dep_d <= 0 || c->dep_layers <= 0 || c->dep_heads <= 0 || c->dep_ffn <= 0) return false;
+  if (c->dep_d % c->dep_heads || !head_dim_ok(c->dep_d / c->dep_heads)) return false;
+  if (c->dep_heads > 32) return false;  // one warp per depformer head in one CTA
+  if (c->n_q != 16 || c->text_vocab <= 0 || c->audio_card <= 0) return false;
+  if (c->window <= 0 || c->max_batch <= 0 || c->max_batch > kMaxBatch) return false;
+  // 16-byte rows for the vectorised weight and activation streams
+  if (c->d_model % 8 || c->ffn % 8 || c->dep_d % 8 || c->dep_ffn % 8) return false;
+  if (!(c->eps > 0.f) || !(c->rope_base > 1.f)) return false;
+  return true;
+}
+
+Dims make_dims(const pp_config* c) {
+  Dims D;
+  D.d = c->d_model; D.L = c->n_layers; D.H = c->n_heads; D.Dh = c->d_model / c->n_heads;
+  D.F = c->ffn; D.Vt = c->text_vocab; D.Va = c->audio_card; D.nq = c->n_q;
+  D.dd = c->dep_d; D.Ld = c->dep_layers; D.Hd = c->dep_heads; D.Dhd = c->dep_d / c->dep_heads;
+  D.Fd = c->dep_ffn; D.W = c->window; D.B = c->max_batch;
+  D.eps = c->eps; D.rope_base = c->rope_base;
+  D.nc_max = (c->window + kAttnChunk - 1) / kAttnChunk;
+  D.logits_ld = c->text_vocab + c->n_q * c->audio_card;
+  return D;
+}
+
+// Workspace carve-up: every region 256-byte aligned, in a fixed order.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~(size_t)255;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+size_t carve(const Dims& D, char* base, Buffers* b) {
+  Carver cv{base};
+  const size_t B = D.B;
+  const size_t wide = D.d > D.F ? D.d : D.F;
+  const size_t dwide = D.dd > D.Fd ? D.dd : D.Fd;
+  b->ring = cv.take<uint16_t>((size_t)D.L * B * 2 * D.H * D.W * D.Dh);
+  b->pos = cv.take<int32_t>(B);
+  b->live = cv.take<int32_t>(B);
+  b->ctl = cv.take<int32_t>(B);
+  b->ctl_pos = cv.take<int32_t>(B);
+  b->status = cv.take<uint32_t>(1);
+  b->attn_count = cv.take<uint32_t>(B * D.H);
+  b->in_col = cv.take<int32_t>(B * kRows);
+  b->in_user = cv.take<int32_t>(B * PP_USER_ROWS);
+  b->in_fmask = cv.take<uint8_t>(B * kRows);
+  b->in_forced = cv.take<int32_t>(B * kRows);
+  b->out_col = cv.take<int32_t>(B * kRows);
+  b->x = cv.take<float>(B * D.d);
+  b->xn = cv.take<float>(B * wide);
+  b->z = cv.take<float>(B * D.d);
+  b->qkv = cv.take<float>(B * 3 * D.d);
+  b->q = cv.take<float>(B * D.d);
+  b->o = cv.take<float>(B * D.d);
+  b->hmlp = cv.take<float>(B * D.F);
+  b->rope_cs = cv.take<float>(B * D.Dh);
+  b->attn_part = cv.take<float>(B * D.H * D.nc_max * (D.Dh + 2));
+  b->logits = cv.take<float>(B * D.logits_ld);
+  b->tok = cv.take<int32_t>(B);
+  b->y = cv.take<float>(B * D.dd);
+  b->yn = cv.take<float>(B * dwide);
+  b->dqkv = cv.take<float>(B * 3 * D.dd);
+  b->dkv = cv.take<float>(B * D.Ld * D.nq * 2 * D.dd);
+  b->dout = cv.take<float>(B * D.dd);
+  b->dh = cv.take<float>(B * D.Fd);
+  return (cv.off + 255) & ~(size_t)255;
+}
+
+#define PP_TRY(x)                         \
+  do {                                    \
+    cudaError_t err_ = (x);               \
+    if (err_ != cudaSuccess) return err_; \
+  } while (0)
+
+// The whole tick, in stream order.  With prof != nullptr a timing event is recorded
+// before every launch (and once at the end).
+#define MARK(k)                                 \
+  do {                                          \
+    if (prof) PP_TRY(prof->mark((k), s));       \
+  } while (0)
+
+cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* prof) {
+  MARK(PP_K_BEGIN);
+  PP_TRY(launch_begin(D, b, s));
+  for (int l = 0; l < D.L; ++l) {
+    MARK(PP_K_NORM);
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, b.xn, D.d, s));
+    GemvArgs a{};
+    a.W = b.wqkv + (size_t)l * 3 * D.d * D.d; a.M = 3 * D.d; a.K = D.d;
+    a.X = b.xn; a.ldx = D.d; a.Y = b.qkv; a.ldy = 3 * D.d; a.epi = EPI_STORE;
+    MARK(PP_K_QKV);
+    PP_TRY(launch_gemv(D, a, s));
+    MARK(PP_K_ROPE_RING);
+    PP_TRY(launch_rope_ring(D, b, l, s));
+    MARK(PP_K_ATTN);
+    PP_TRY(launch_attn(D, b, l, s));
+    a = GemvArgs{};
+    a.W = b.wo + (size_t)l * D.d * D.d; a.M = D.d; a.K = D.d;
+    a.X = b.o; a.ldx = D.d; a.Y = b.x; a.ldy = D.d; a.epi = EPI_ADD;
+    MARK(PP_K_OPROJ);
+    PP_TRY(launch_gemv(D, a, s));
+    MARK(PP_K_NORM);
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.mlp_alpha + (size_t)l * D.d, D.d, b.xn, D.d, s));
+    a = GemvArgs{};
+    a.W = b.wgu + (size_t)l * 2 * D.F * D.d; a.M = D.F; a.K = D.d;
+    a.X = b.xn; a.ldx = D.d; a.Y = b.hmlp; a.ldy = D.F; a.epi = EPI_SILU;
+    MARK(PP_K_GATEUP);
+    PP_TRY(launch_gemv(D, a, s));
+    a = GemvArgs{};
+    a.W = b.wdown + (size_t)l * D.d * D.F; a.M = D.d; a.K = D.F;
+    a.X = b.hmlp; a.ldx = D.F; a.Y = b.x; a.ldy = D.d; a.epi = EPI_ADD;
+    MARK(PP_K_DOWN);
+    PP_TRY(launch_gemv(D, a, s));
+  }
+  MARK(PP_K_TEXT_HEAD);
+  PP_TRY(launch_rmsnorm(D, b.x, D.d, b.out_alpha, D.d, b.z, D.d, s));
+  {
+    GemvArgs a{};
+    a.W = b.wtext; a.M = D.Vt; a.K = D.d;
+    a.X = b.z; a.ldx = D.d; a.Y = b.logits; a.ldy = D.logits_ld; a.epi = EPI_STORE;
+    MARK(PP_K_TEXT_HEAD);
+    PP_TRY(launch_gemv(D, a, s));
+  }
+  MARK(PP_K_TEXT_HEAD);
+  PP_TRY(launch_text_argmax(D, b, s));
+  for (int k = 0; k < D.nq; ++k) {
+    GemvArgs a{};
+    a.W = b.dep_inproj + (size_t)k * D.dd * D.d; a.M = D.dd; a.K = D.d;
+    a.X = b.z; a.ldx = D.d; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_EMB;
+    a.emb = (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
+    a.tok = b.tok;
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+    for (int j = 0; j < D.Ld; ++j) {
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, s));
+      a = GemvArgs{};
+      a.W = b.dep_wqkv + (size_t)j * 3 * D.dd * D.dd; a.M = 3 * D.dd; a.K = D.dd;
+      a.X = b.yn; a.ldx = D.dd; a.Y = b.dqkv; a.ldy = 3 * D.dd; a.epi = EPI_STORE;
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_dep_attn(D, b, k, j, s));
+      a = GemvArgs{};
+      a.W = b.dep_wo + (size_t)j * D.dd * D.dd; a.M = D.dd; a.K = D.dd;
+      a.X = b.dout; a.ldx = D.dd; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_ADD;
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, s));
+      a = GemvArgs{};
+      a.W = b.dep_wgu + (size_t)j * 2 * D.Fd * D.dd; a.M = D.Fd; a.K = D.dd;
+      a.X = b.yn; a.ldx = D.dd; a.Y = b.dh; a.ldy = D.Fd; a.epi = EPI_SILU;
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+      a = GemvArgs{};
+      a.W = b.dep_wdown + (size_t)j * D.dd * D.Fd; a.M = D.dd; a.K = D.Fd;
+      a.X = b.dh; a.ldx = D.Fd; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_ADD;
+      MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+    }
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, b.yn, D.dd, s));
+    a = GemvArgs{};
+    a.W = b.dep_heads + (size_t)k * D.Va * D.dd; a.M = D.Va; a.K = D.dd;
+    a.X = b.yn; a.ldx = D.dd; a.Y = b.logits + D.Vt + (size_t)k * D.Va; a.ldy = D.logits_ld;
+    a.epi = EPI_STORE;
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_gemv(D, a, s));
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_dep_argmax(D, b, k, s));
+  }
+  MARK(PP_K_FINISH);
+  PP_TRY(launch_finish(D, b, s));
+  MARK(PP_K_COUNT);   // end marker
+  return cudaSuccess;
+}
+
+int weight_dims(const pp_config* c, int which, int64_t d[4], int* nd, int* f32) {
+  const int64_t dm = c->d_model, L = c->n_layers, F = c->ffn, Vt = c->text_vocab,
+                Va = c->audio_card, nq = c->n_q, dd = c->dep_d, Ld = c->dep_layers,
+                Fd = c->dep_ffn;
+  *f32 = 0;
+  auto set = [&](int n, int64_t a, int64_t b2, int64_t c2) {
+    *nd = n; d[0] = a; d[1] = b2; d[2] = c2; d[3] = 0;
+  };
+  switch (which) {
+    case PP_W_EMB_TEXT: set(2, Vt + 1, dm, 0); break;
+    case PP_W_EMB_AUDIO: set(3, nq, Va + 1, dm); break;
+    case PP_W_ATTN_ALPHA: set(2, L, dm, 0); *f32 = 1; break;
+    case PP_W_QKV: set(3, L, 3 * dm, dm); break;
+    case PP_W_O: set(3, L, dm, dm); break;
+    case PP_W_MLP_ALPHA: set(2, L, dm, 0); *f32 = 1; break;
+    case PP_W_GU: set(3, L, 2 * F, dm); break;
+    case PP_W_DOWN: set(3, L, dm, F); break;
+    case PP_W_OUT_ALPHA: set(1, dm, 0, 0); *f32 = 1; break;
+    case PP_W_TEXT: set(2, Vt, dm, 0); break;
+    case PP_W_DEP_INPROJ: set(3, nq, dd, dm); break;
+    case PP_W_DEP_EMB_TEXT: set(2, Vt + 1, dd, 0); break;
+    case PP_W_DEP_EMB_AUDIO: set(3, nq - 1, Va + 1, dd); break;
+    case PP_W_DEP_ATTN_ALPHA: set(2, Ld, dd, 0); *f32 = 1; break;
+    case PP_W_DEP_QKV: set(3, Ld, 3 * dd, dd); break;
+    case PP_W_DEP_O: set(3, Ld, dd, dd); break;
+    case PP_W_DEP_MLP_ALPHA: set(2, Ld, dd, 0); *f32 = 1; break;
+    case PP_W_DEP_GU: set(3, Ld, 2 * Fd, dd); break;
+    case PP_W_DEP_DOWN: set(3, Ld, dd, Fd); break;
+    case PP_W_DEP_OUT_ALPHA: set(1, dd, 0, 0); *f32 = 1; break;
+    case PP_W_DEP_HEADS: set(3, nq, Va, dd); break;
+    default: return PP_EINVAL;
+  }
+  return PP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pp_weight_shape(const pp_config* c, int which, int64_t dims[4], int* ndim, int* is_f32) {
+  if (!config_ok(c) || !dims || !ndim || !is_f32) return PP_EINVAL;
+  return weight_dims(c, which, dims, ndim, is_f32);
+}
+
+size_t pp_workspace_bytes(const pp_config* c) {
+  if (!config_ok(c)) return 0;
+  Buffers b{};
+  return carve(make_dims(c), nullptr, &b);
+}
+
+int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t ws_bytes,
+              pp_engine** out) {
+  if (!out) return PP_EINVAL;
+  *out = nullptr;
+  if (!config_ok(c) || !w || !workspace) return PP_EINVAL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return PP_EINVAL;
+  for (int i = 0; i < PP_W_COUNT; ++i)
+    if (!w->ptr[i] || (reinterpret_cast<uintptr_t>(w->ptr[i]) & 15)) return PP_EINVAL;
+  const Dims D = make_dims(c);
+  Buffers b{};
+  const size_t need = carve(D, reinterpret_cast<char*>(workspace), &b);
+  if (ws_bytes < need) return PP_E_NOSPACE;
+  b.emb_text = (const uint16_t*)w->ptr[PP_W_EMB_TEXT];
+  b.emb_audio = (const uint16_t*)w->ptr[PP_W_EMB_AUDIO];
+  b.attn_alpha = (const float*)w->ptr[PP_W_ATTN_ALPHA];
+  b.wqkv = (const uint16_t*)w->ptr[PP_W_QKV];
+  b.wo = (const uint16_t*)w->ptr[PP_W_O];
+  b.mlp_alpha = (const float*)w->ptr[PP_W_MLP_ALPHA];
+  b.wgu = (const uint16_t*)w->ptr[PP_W_GU];
+  b.wdown = (const uint16_t*)w->ptr[PP_W_DOWN];
+  b.out_alpha = (const float*)w->ptr[PP_W_OUT_ALPHA];
+  b.wtext = (const uint16_t*)w->ptr[PP_W_TEXT];
+  b.dep_inproj = (const uint16_t*)w->ptr[PP_W_DEP_INPROJ];
+  b.dep_emb_text = (const uint16_t*)w->ptr[PP_W_DEP_EMB_TEXT];
+  b.dep_emb_audio = (const uint16_t*)w->ptr[PP_W_DEP_EMB_AUDIO];
+  b.dep_attn_alpha = (const float*)w->ptr[PP_W_DEP_ATTN_ALPHA];
+  b.dep_wqkv = (const uint16_t*)w->ptr[PP_W_DEP_QKV];
+  b.dep_wo = (const uint16_t*)w->ptr[PP_W_DEP_O];
+  b.dep_mlp_alpha = (const float*)w->ptr[PP_W_DEP_MLP_ALPHA];
+  b.dep_wgu = (const uint16_t*)w->ptr[PP_W_DEP_GU];
+  b.dep_wdown = (const uint16_t*)w->ptr[PP_W_DEP_DOWN];
+  b.dep_out_alpha = (const float*)w->ptr[PP_W_DEP_OUT_ALPHA];
+  b.dep_heads = (const uint16_t*)w->ptr[PP_W_DEP_HEADS];
+
+  pp_engine* e = new (std::nothrow) pp_engine();
+  if (!e) return PP_EINVAL;
+  e->cfg = *c;
+  e->D = D;
+  e->buf = b;
+  e->ctl.assign(D.B, 0);
+  e->ctl_pos.assign(D.B, 0);
+  e->pos.assign(D.B, 0);
+  e->open.assign(D.B, 0);
+
+  cudaError_t err = cudaSuccess;
+  // zero the small state (positions, liveness, control, status, attention counters)
+  char* small_lo = reinterpret_cast<char*>(b.pos);
+  char* small_hi = reinterpret_cast<char*>(b.in_col);
+  err = cudaMemset(small_lo, 0, (size_t)(small_hi - small_lo));
+  if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking);
+  if (err == cudaSuccess)
+    err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
+  if (err == cudaSuccess) {
+    cudaError_t le = enqueue_tick(e->D, e->buf, e->cap_stream, nullptr);
+    err = cudaStreamEndCapture(e->cap_stream, &e->graph);
+    if (le != cudaSuccess) err = le;
+  }
+  if (err == cudaSuccess) err = cudaGraphInstantiate(&e->exec, e->graph, 0);
+  if (err == cudaSuccess) {
+    size_t n = 0;
+    err = cudaGraphGetNodes(e->graph, nullptr, &n);
+    e->n_kernels = (int)n;
+  }
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) {
+    pp_destroy(e);
+    return PP_E_CUDA;
+  }
+  *out = e;
+  return PP_OK;
+}
+
+void pp_destroy(pp_engine* e) {
+  if (!e) return;
+  if (e->prof_exec) cudaGraphExecDestroy(e->prof_exec);
+  if (e->prof_graph) cudaGraphDestroy(e->prof_graph);
+  e->prof.clear();
+  if (e->exec) cudaGraphExecDestroy(e->exec);
+  if (e->graph) cudaGraphDestroy(e->graph);
+  if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+  delete e;
+}
+
+static int open_at(pp_engine* e, int slot, int64_t pos) {
+  if (!e) return PP_EINVAL;
+  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (pos < 0 || pos >= 0x7FFFFFFF) return PP_E_RANGE;
+  if (e->open[slot]) return PP_E_BUSY;
+  e->open[slot] = 1;
+  e->ctl[slot] = 1 | 2;
+  e->ctl_pos[slot] = (int32_t)pos;
+  e->ctl_dirty = true;
+  e->pos[slot] = pos;
+  return PP_OK;
+}
+
+int pp_session_open(pp_engine* e, int slot) { return open_at(e, slot, 0); }
+
+int pp_session_import(pp_engine* e, int slot, int64_t pos) { return open_at(e, slot, pos); }
+
+int pp_session_close(pp_engine* e, int slot) {
+  if (!e) return PP_EINVAL;
+  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (!e->open[slot]) return PP_E_NOTLIVE;
+  e->open[slot] = 0;
+  e->ctl[slot] = 0;
+  e->ctl_dirty = true;
+  return PP_OK;
+}
+
+int pp_session_pos(pp_engine* e, int slot, int64_t* pos) {
+  if (!e || !pos) return PP_EINVAL;
+  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (!e->open[slot]) return PP_E_NOTLIVE;
+  *pos = e->pos[slot];
+  return PP_OK;
+}
+
+int pp_ring_block(pp_engine* e, int layer, int slot, int kv, void** ptr) {
+  if (!e || !ptr || (kv != 0 && kv != 1)) return PP_EINVAL;
+  if (layer < 0 || layer >= e->D.L || slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  const Dims& D = e->D;
+  *ptr = e->buf.ring + ((((size_t)layer * D.B + slot) * 2 + kv) * D.H) * (size_t)D.W * D.Dh;
+  return PP_OK;
+}
+
+static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+                     const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+                     float* logits, cudaStream_t s, bool wait, cudaGraphExec_t exec) {
+  if (!e || !prev_column || !user_codes || !column) return PP_EINVAL;
+  if ((force_mask != nullptr) != (forced_tokens != nullptr)) return PP_EINVAL;
+  const Dims& D = e->D;
+  const Buffers& b = e->buf;
+  const size_t B = D.B;
+  cudaError_t err = cudaMemcpyAsync(b.in_col, prev_column, B * kRows * 4, cudaMemcpyDefault, s);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(b.in_user, user_codes, B * PP_USER_ROWS * 4, cudaMemcpyDefault, s);
+  if (err == cudaSuccess) {
+    if (force_mask) {
+      err = cudaMemcpyAsync(b.in_fmask, force_mask, B * kRows, cudaMemcpyDefault, s);
+      if (err == cudaSuccess)
+        err = cudaMemcpyAsync(b.in_forced, forced_tokens, B * kRows * 4, cudaMemcpyDefault, s);
+    } else {
+      err = cudaMemsetAsync(b.in_fmask, 0, B * kRows, s);
+    }
+  }
+  // control words, only after an open/close: pageable host memory is staged by the
+  // runtime before the call returns, so the host copy may change right after
+  const bool upload = e->ctl_dirty;
+  if (err == cudaSuccess && upload)
+    err = cudaMemcpyAsync(b.ctl, e->ctl.data(), B * 4, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess && upload)
+    err = cudaMemcpyAsync(b.ctl_pos, e->ctl_pos.data(), B * 4, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaGraphLaunch(exec, s);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(column, b.out_col, B * kRows * 4, cudaMemcpyDefault, s);
+  if (err == cudaSuccess && logits)
+    err = cudaMemcpyAsync(logits, b.logits, B * (size_t)D.logits_ld * 4, cudaMemcpyDefault, s);
+  if (err == cudaSuccess && wait) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return PP_E_CUDA;
+  if (upload) {
+    for (size_t i = 0; i < B; ++i) e->ctl[i] &= 1;   // the device applies a reset once
+    e->ctl_dirty = false;
+  }
+  for (size_t i = 0; i < B; ++i)
+    if (e->open[i]) e->pos[i] += 1;
+  return PP_OK;
+}
+
+int pp_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+            const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+            float* logits, void* stream) {
+  if (!e) return PP_EINVAL;
+  return step_impl(e, prev_column, user_codes, force_mask, forced_tokens, column, logits,
+                   (cudaStream_t)stream, false, e->exec);
+}
+
+int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+                 const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+                 float* logits, void* stream) {
+  if (!e) return PP_EINVAL;
+  return step_impl(e, prev_column, user_codes, force_mask, forced_tokens, column, logits,
+                   (cudaStream_t)stream, true, e->exec);
+}
+
+int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+                    const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+                    float* logits, void* stream, double* kind_ms, int64_t* kind_launches) {
+  if (!e || !kind_ms || !kind_launches) return PP_EINVAL;
+  if (!e->prof_exec) {   // capture the profiling graph on first use
+    cudaError_t err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
+    if (err == cudaSuccess) {
+      cudaError_t le = enqueue_tick(e->D, e->buf, e->cap_stream, &e->prof);
+      err = cudaStreamEndCapture(e->cap_stream, &e->prof_graph);
+      if (le != cudaSuccess) err = le;
+    }
+    if (err == cudaSuccess) err = cudaGraphInstantiate(&e->prof_exec, e->prof_graph, 0);
+    if (err != cudaSuccess) {
+      if (e->prof_graph) cudaGraphDestroy(e->prof_graph);
+      e->prof_graph = nullptr;
+      e->prof.clear();
+      return PP_E_CUDA;
+    }
+  }
+  int rc = step_impl(e, prev_column, user_codes, force_mask, forced_tokens, column, logits,
+                     (cudaStream_t)stream, true, e->prof_exec);
+  if (rc != PP_OK) return rc;
+  const size_t n = e->prof.ev.size();
+  for (size_t i = 0; i + 1 < n; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, e->prof.ev[i], e->prof.ev[i + 1]) != cudaSuccess)
+      return PP_E_CUDA;
+    const int k = e->prof.kind[i];
+    if (k >= 0 && k < PP_K_COUNT) {
+      kind_ms[k] += ms;
+      kind_launches[k] += 1;
+    }
+  }
+  return PP_OK;
+}
+
+int pp_status(pp_engine* e, void* stream, uint32_t* bits) {
+  if (!e || !bits) return PP_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  cudaError_t err = cudaStreamSynchronize(s);
+  if (err == cudaSuccess) err = cudaMemcpy(&v, e->buf.status, 4, cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess) err = cudaMemset(e->buf.status, 0, 4);
+  if (err == cudaSuccess) err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return PP_E_CUDA;
+  *bits = v;
+  return PP_OK;
+}
+
+int pp_step_kernel_count(pp_engine* e) { return e ? e->n_kernels : PP_EINVAL; }
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+// pp_internal.cuh - engine layout and kernel launchers of the lockstep tick (sm_103a).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pp.h"
+
+namespace pp {
+
+constexpr int kRows = PP_ROWS;
+constexpr int kAttnChunk = 256;     // ring positions per attention CTA (split-K unit)
+constexpr int kAttnWarps = 8;       // 32 positions per warp
+constexpr int kMaxBatch = 64;
+
+// Device-side pointers and sizes every kernel of the tick needs.
+struct Dims {
+  int d, L, H, Dh, F, Vt, Va, nq, dd, Ld, Hd, Dhd, Fd, W, B;
+  float eps, rope_base;
+  int nc_max;            // attention chunks per (slot, head) at a full ring
+  int logits_ld;         // Vt + nq * Va
+  int Bp;                // slots padded to a multiple of 8: operand rows are [hi: Bp][lo: Bp]
+};
+
+struct Buffers {
+  // weights
+  const uint16_t* emb_text;
+  const uint16_t* emb_audio;
+  const float* attn_alpha;
+  const uint16_t* wqkv;
+  const uint16_t* wo;
+  const float* mlp_alpha;
+  const uint16_t* wgu;
+  const uint16_t* wdown;
+  const float* out_alpha;
+  const uint16_t* wtext;
+  const uint16_t* dep_inproj;
+  const uint16_t* dep_emb_text;
+  const uint16_t* dep_emb_audio;
+  const float* dep_attn_alpha;
+  const uint16_t* dep_wqkv;
+  const uint16_t* dep_wo;
+  const float* dep_mlp_alpha;
+  const uint16_t* dep_wgu;
+  const uint16_t* dep_wdown;
+  const float* dep_out_alpha;
+  const uint16_t* dep_heads;
+  // state
+  uint16_t* ring;          // [L][B][2][H][W][Dh] bf16
+  int32_t* pos;            // [B]
+  int32_t* live;           // [B]
+  int32_t* ctl;            // [B] host-uploaded control: bit0 live, bit1 reset position
+  int32_t* ctl_pos;        // [B] position applied when bit1 is set
+  uint32_t* status;        // [1]
+  // per-tick inputs / outputs (staged)
+  int32_t* in_col;         // [B][17]
+  int32_t* in_user;        // [B][8]
+  uint8_t* in_fmask;       // [B][17]
+  int32_t* in_forced;      // [B][17]
+  int32_t* out_col;        // [B][17]
+  // activations and scratch
+  float* x;                // [B][d]
+  float* xn;               // [B][max(d, F)] normalised input of the next contraction
+  float* z;                // [B][d] post final norm (text head and depformer input)
+  float* qkv;              // [B][3d]
+  float* q;                // [B][d] rotated, pre-scaled query
+  float* o;                // [B][d]
+  float* hmlp;             // [B][F]
+  float* rope_cs;          // [B][Dh/2][2]
+  float* attn_part;        // [B][H][nc_max][Dh+2]
+  uint32_t* attn_count;    // [B][H]
+  float* logits;           // [B][logits_ld]
+  int32_t* tok;            // [B] token feeding the next depformer step
+  float* y;                // [B][dd]
+  float* yn;               // [B][max(dd, Fd)]
+  float* dqkv;             // [B][3dd]
+  float* dkv;              // [B][Ld][nq][2][dd]
+  float* dout;             // [B][dd]
+  float* dh;               // [B][Fd]
+  // bf16 hi/lo activation operands of the tensor-core contractions, [2*Bp][K]
+  uint16_t* op_d;          // K = d   (normalised temporal stream)
+  uint16_t* op_o;          // K = d   (attention output)
+  uint16_t* op_f;          // K = F   (gated MLP hidden)
+  uint16_t* op_z;          // K = d   (post final norm: text head and depformer input)
+  uint16_t* op_dd;         // K = dd  (normalised depformer stream)
+  uint16_t* op_do;         // K = dd  (depformer attention output)
+  uint16_t* op_fd;         // K = Fd  (depformer gated hidden)
+  float* partial;          // split-K partials of the tensor-core contractions
+  uint32_t* tile_count;    // split-K tickets per M-tile
+};
+
+constexpr int kMaxUnits = 2048;      // cap on (M-tile x K-split) units of one contraction
+constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction (ticket array)
+
+// ---- launchers (stream-ordered; return cudaGetLastError) ----------------------------
+cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s);
+// out (fp32, may be null) and/or op (bf16 hi/lo operand [2*Bp][K], may be null)
+cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
+                           float* out, int ldo, uint16_t* op, cudaStream_t s);
+
+// hi/lo split of v into operand row b (hi) and Bp + b (lo), column k
+__device__ __forceinline__ void op_store(uint16_t* op, int ld, int Bp, int b, int k, float v) {
+  uint32_t u = __float_as_uint(v);
+  uint32_t h = (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : ((u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u);
+  const float rem = v - __uint_as_float(h);
+  uint32_t r = __float_as_uint(rem);
+  r = (r & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : r + 0x7FFFu + ((r >> 16) & 1u);
+  op[(size_t)b * ld + k] = (uint16_t)(h >> 16);
+  op[(size_t)(Bp + b) * ld + k] = (uint16_t)(r >> 16);
+}
+
+// Tensor-core contraction (k_umma.cu).
+struct UmmaArgs {
+  int M;               // output rows (EPI_SILU: number of gate/up pairs)
+  int pair_rows;       // EPI_SILU: F, the up rows start pair_rows after the gate rows; else 0
+  int row0;            // first row of this matrix in the stacked weight tensor map
+  int kblocks;         // ceil(K / 64)
+  int splits;          // K-splits per M-tile (depends on shape and SM count only)
+  int m_tiles;
+  int B;               // slots
+  int N;               // MMA N = 2 * Bp
+  int epi;
+  float* Y;            // EPI_STORE / EPI_ADD / EPI_EMB output [B][ldy]
+  int ldy;
+  const uint16_t* emb; // EPI_EMB table [rows][M]
+  const int32_t* tok;
+  uint16_t* op_out;    // EPI_SILU: operand [2*Bp_out][ld_op] of the next contraction
+  int ld_op;
+  int Bp_out;
+  float* partial;
+  uint32_t* counter;
+  uint32_t* status;
+};
+cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
+                        cudaStream_t s);
+cudaError_t umma_setup(int N);
+int umma_stage_count(int N);
+
+enum GemvEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_EMB = 3 };
+struct GemvArgs {
+  const uint16_t* W;     // [M, K] bf16 (EPI_SILU: [2M, K], gate rows then up rows)
+  int M, K;
+  const float* X;        // [B, ldx] fp32
+  int ldx;
+  float* Y;              // [B, ldy] fp32
+  int ldy;
+  int epi;
+  const uint16_t* emb;   // EPI_EMB: table [rows, M] bf16, row tok[b]
+  const int32_t* tok;    // EPI_EMB
+};
+cudaError_t launch_gemv(const Dims& D, const GemvArgs& a, cudaStream_t s);
+
+cudaError_t launch_rope_ring(const Dims& D, const Buffers& b, int layer, cudaStream_t s);
+cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s);
+cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
+cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
+                            cudaStream_t s);
+cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s);
+cudaError_t launch_finish(const Dims& D, const Buffers& b, cudaStream_t s);
+
+}  // namespace pp

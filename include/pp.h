@@ -1,0 +1,208 @@
+/*
+ * pp.h - C ABI of the GB300 (sm_103a) lockstep decode tick of the PersonaPlex / Moshi
+ * RQ-Transformer: one 80 ms step for up to max_batch concurrent full-duplex sessions.
+ *
+ * What one step computes (vllm-omni recipes/NVIDIA/PersonaPlex.md, "Architecture";
+ * "PersonaPlex 全双工语音对话实战 ... 80ms Lockstep", sections 架构 and 帧 token 布局):
+ *   1. x = text_table[col[0]] + sum_{r=1..16} audio_table[r-1][col[r]] over the
+ *      previous column (row 0 inner-monologue text, rows 1-8 agent audio, rows 9-16
+ *      user audio);
+ *   2. the Helium temporal transformer (fp32-alpha RMSNorm, fused QKV in-projection,
+ *      interleaved RoPE at the slot's absolute position, attention over the slot's
+ *      ring KV cache with a sliding window, SiLU-gated MLP);
+ *   3. the greedy text token (lowest index on ties) unless forced;
+ *   4. the depformer: 16 autoregressive codebook steps with a cache reset every frame;
+ *      agent rows 1-8 greedy unless forced, user rows 9-16 always the incoming codes.
+ * Persona and voice prefill are ordinary steps with forced tokens.
+ *
+ * Conventions
+ *  - Every array is indexed by slot: [max_batch, ...], row-major.  Slots that are not
+ *    open are ignored on input and produce column rows of -1 on output.
+ *  - Weights and workspace are caller-owned device memory; the engine never frees
+ *    them and they must outlive the engine.  Matrices are row-major [out, in] bf16
+ *    (PyTorch Linear orientation); per-layer tensors are stacked along a leading axis.
+ *  - Return value: PP_OK (0) or a negative PP_E* code, detected synchronously on the
+ *    host.  Conditions found on the device (NaN logits, out-of-range tokens, timed-out
+ *    waits) are OR-ed into a device status word read by pp_status.
+ *  - A stream argument is a cudaStream_t passed as void* (NULL = legacy default stream).
+ */
+#ifndef PP_H
+#define PP_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PP_ROWS 17           /* rows of one column: text, 8 agent codebooks, 8 user codebooks */
+#define PP_AGENT_ROWS 8
+#define PP_USER_ROWS 8
+
+/* host-detected errors */
+#define PP_OK 0
+#define PP_EINVAL (-1)       /* bad argument or config */
+#define PP_E_BUSY (-2)       /* slot already open */
+#define PP_E_RANGE (-3)      /* slot, layer or position out of range */
+#define PP_E_NOTLIVE (-4)    /* slot not open */
+#define PP_E_CUDA (-5)       /* a CUDA runtime call failed */
+#define PP_E_NOSPACE (-6)    /* workspace smaller than pp_workspace_bytes */
+
+/* device-detected conditions (bits of the status word) */
+#define PP_S_NAN 0x1u        /* a logit row held NaN (the NaN entries were not chosen) */
+#define PP_S_INDEX 0x2u      /* an input token was out of range (replaced by the initial token) */
+#define PP_S_TIMEOUT 0x4u    /* a bounded device-side wait gave up */
+
+typedef struct {
+  int32_t d_model;       /* 4096 */
+  int32_t n_layers;      /* 32 */
+  int32_t n_heads;       /* 32; head dim = d_model / n_heads, one of 32, 64, 128 */
+  int32_t ffn;           /* 11008 */
+  int32_t text_vocab;    /* 32000 text logits; text tables have text_vocab+1 rows, the
+                            last being TEXT_INITIAL_TOKEN = text_vocab */
+  int32_t audio_card;    /* 2048 codes; audio tables have audio_card+1 rows, the last
+                            being AUDIO_INITIAL_TOKEN = audio_card */
+  int32_t n_q;           /* 16 audio rows = depformer steps (must be 16) */
+  int32_t dep_d;         /* 1024 */
+  int32_t dep_layers;    /* 6 */
+  int32_t dep_heads;     /* 16; head dim = dep_d / dep_heads, one of 32, 64, 128 */
+  int32_t dep_ffn;       /* depformer FFN width */
+  int32_t window;        /* 3000 ring positions per slot */
+  int32_t max_batch;     /* slots, 1..64 */
+  float eps;             /* RMSNorm epsilon (inside the square root) */
+  float rope_base;       /* RoPE base (10000) */
+} pp_config;
+
+/* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
+ * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */
+enum pp_weight {
+  PP_W_EMB_TEXT = 0,     /* bf16 [Vt+1, d] */
+  PP_W_EMB_AUDIO,        /* bf16 [n_q, Va+1, d]       (row r of a column uses table r-1) */
+  PP_W_ATTN_ALPHA,       /* f32  [L, d] */
+  PP_W_QKV,              /* bf16 [L, 3d, d]           rows: q heads, k heads, v heads */
+  PP_W_O,                /* bf16 [L, d, d] */
+  PP_W_MLP_ALPHA,        /* f32  [L, d] */
+  PP_W_GU,               /* bf16 [L, 2F, d]           rows: gate (F) then up (F) */
+  PP_W_DOWN,             /* bf16 [L, d, F] */
+  PP_W_OUT_ALPHA,        /* f32  [d] */
+  PP_W_TEXT,             /* bf16 [Vt, d] */
+  PP_W_DEP_INPROJ,       /* bf16 [n_q, dd, d]         per-codebook input projection */
+  PP_W_DEP_EMB_TEXT,     /* bf16 [Vt+1, dd]           step 0 token table */
+  PP_W_DEP_EMB_AUDIO,    /* bf16 [n_q-1, Va+1, dd]    step k >= 1 uses table k-1 */
+  PP_W_DEP_ATTN_ALPHA,   /* f32  [Ld, dd] */
+  PP_W_DEP_QKV,          /* bf16 [Ld, 3dd, dd] */
+  PP_W_DEP_O,            /* bf16 [Ld, dd, dd] */
+  PP_W_DEP_MLP_ALPHA,    /* f32  [Ld, dd] */
+  PP_W_DEP_GU,           /* bf16 [Ld, 2Fd, dd] */
+  PP_W_DEP_DOWN,         /* bf16 [Ld, dd, Fd] */
+  PP_W_DEP_OUT_ALPHA,    /* f32  [dd] */
+  PP_W_DEP_HEADS,        /* bf16 [n_q, Va, dd]        per-codebook output head */
+  PP_W_COUNT
+};
+
+typedef struct {
+  const void* ptr[PP_W_COUNT];  /* device pointers, 16-byte aligned */
+} pp_weights;
+
+typedef struct pp_engine pp_engine;  /* opaque */
+
+/* Shape of weight tensor `which` for config c: dims[0..*ndim-1], *is_f32 = 1 for the
+ * fp32 alpha vectors, 0 for bf16.  Returns PP_EINVAL for a bad config or index. */
+int pp_weight_shape(const pp_config* c, int which, int64_t dims[4], int* ndim, int* is_f32);
+
+/* Bytes of device workspace the engine needs for config c (ring KV for every slot,
+ * activations, per-step scratch, status word), or 0 for a bad config. */
+size_t pp_workspace_bytes(const pp_config* c);
+
+/* Create an engine.  w: device weight pointers (not copied, must outlive the engine).
+ * workspace: device memory of at least pp_workspace_bytes(c) bytes, 256-byte aligned,
+ * owned by the caller.  Captures the whole tick as one CUDA graph.  All slots start
+ * closed.  Errors: PP_EINVAL, PP_E_NOSPACE, PP_E_CUDA. */
+int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t ws_bytes,
+              pp_engine** out);
+
+void pp_destroy(pp_engine* e);
+
+/* Open slot `slot` for a new session at position 0 (the slot's ring contents are
+ * ignored from then on because attention reads only positions written since open;
+ * a recycled slot behaves exactly like a fresh engine).  Takes effect at the next
+ * pp_step.  Errors: PP_E_RANGE (slot >= max_batch), PP_E_BUSY (already open). */
+int pp_session_open(pp_engine* e, int slot);
+
+/* Close slot `slot` at the next pp_step.  Errors: PP_E_RANGE, PP_E_NOTLIVE. */
+int pp_session_close(pp_engine* e, int slot);
+
+/* Open slot `slot` resuming a session at absolute position pos (0 <= pos < 2^31-1):
+ * the caller has already written the session's ring contents through pp_ring_block
+ * (ring index j holds the latest position p < pos with p mod window = j).
+ * Errors: PP_E_RANGE, PP_E_BUSY. */
+int pp_session_import(pp_engine* e, int slot, int64_t pos);
+
+/* Current absolute position of an open slot (frames since open), from the host
+ * mirror.  Errors: PP_E_RANGE, PP_E_NOTLIVE. */
+int pp_session_pos(pp_engine* e, int slot, int64_t* pos);
+
+/* Device address of one ring block: layer `layer`, slot `slot`, kv = 0 (K, stored
+ * after RoPE) or 1 (V); the block is bf16 [n_heads, window, head_dim], contiguous.
+ * Errors: PP_E_RANGE, PP_EINVAL. */
+int pp_ring_block(pp_engine* e, int layer, int slot, int kv, void** ptr);
+
+/* One lockstep tick for every open slot, asynchronous on `stream`.  Device pointers:
+ *   prev_column   int32 [max_batch, 17]  the previous column (for a fresh session:
+ *                                         [text_vocab, audio_card x 16])
+ *   user_codes    int32 [max_batch, 8]   this frame's user codes -> rows 9..16
+ *   force_mask    uint8 [max_batch, 17]  nonzero: rows 0..8 take forced_tokens
+ *                                         (rows 9..16 ignore it); may be NULL
+ *   forced_tokens int32 [max_batch, 17]  may be NULL when force_mask is NULL
+ *   column        int32 [max_batch, 17]  out: this frame's column (-1 for closed slots)
+ *   logits        f32 [max_batch, text_vocab + n_q*audio_card] out, or NULL: text
+ *                 logits then the 16 depformer steps' logits
+ * Open slots advance one position.  Errors: PP_EINVAL, PP_E_CUDA. */
+int pp_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+            const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+            float* logits, void* stream);
+
+/* The same tick with HOST buffers (same layouts; pinned memory recommended): copies
+ * the inputs to the device, runs the tick and copies the column (and logits if not
+ * NULL) back, on `stream`, returning after the results are on the host. */
+int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+                 const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+                 float* logits, void* stream);
+
+/* Wait for `stream`, then read and clear the device status word into *bits
+ * (PP_S_* flags).  Errors: PP_E_CUDA. */
+int pp_status(pp_engine* e, void* stream, uint32_t* bits);
+
+/* Number of kernel launches one pp_step makes (the nodes of the captured graph). */
+int pp_step_kernel_count(pp_engine* e);
+
+/* Kernel families of one tick, for pp_profile_step. */
+enum pp_kernel_kind {
+  PP_K_BEGIN = 0,   /* control + 17-table embedding sum + RoPE angle table */
+  PP_K_NORM,        /* RMSNorm of the temporal stream */
+  PP_K_QKV,         /* fused QKV in-projection */
+  PP_K_ROPE_RING,   /* RoPE + ring-KV write */
+  PP_K_ATTN,        /* split-K sliding-window ring attention (+ chunk merge) */
+  PP_K_OPROJ,       /* out-projection + residual */
+  PP_K_GATEUP,      /* gate/up projection + SiLU gating */
+  PP_K_DOWN,        /* down-projection + residual */
+  PP_K_TEXT_HEAD,   /* final norm, text head, greedy text token */
+  PP_K_DEPFORMER,   /* every kernel of the 16 depformer steps */
+  PP_K_FINISH,      /* end-of-tick bookkeeping */
+  PP_K_COUNT
+};
+
+/* pp_step (same arguments) through a second captured graph that records a timing
+ * event at every kernel boundary; waits for the tick, then ADDS each kernel's
+ * duration (ms, event to event, so it includes the launch gap before the next
+ * kernel) to kind_ms[kind] and its launch count to kind_launches[kind] (both arrays of
+ * PP_K_COUNT entries, caller-owned host memory).  For measurement only: slower than
+ * pp_step.  Errors: PP_EINVAL, PP_E_CUDA. */
+int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
+                    const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
+                    float* logits, void* stream, double* kind_ms, int64_t* kind_launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,148 @@
+"""Drives the CUDA path and the CPU oracle side by side on the same seeded inputs.
+
+Used by the GPU parity tests and by ``__graft_entry__.smoke``.  It holds no arithmetic
+of the tick: it schedules sessions, feeds both sides the same inputs and compares.
+
+Teacher forcing: every tick, each open slot of the GPU engine receives the oracle's
+previous column, and rows 0..8 are forced to the oracle's tokens wherever the
+schedule forces them or the oracle's top-2 logit margin is at or below the token gate
+(ties within rounding could go either way on either side).  Everywhere else the GPU
+takes its own greedy decision, which must then equal the oracle's.
+"""
+import dataclasses
+
+import numpy as np
+
+ROWS = 17
+LOGIT_TOL = 2e-2        # max |gpu - oracle| <= LOGIT_TOL * std(oracle logits)
+TOKEN_MARGIN = 1e-2     # tokens must agree where the oracle's top-2 margin exceeds this
+
+
+def top2_margin(v):
+    v = np.asarray(v, np.float32)
+    i = int(np.argmax(v))
+    rest = np.delete(v, i)
+    return float(v[i] - rest.max())
+
+
+def initial_column(shape):
+    return np.array([shape.text_vocab] + [shape.audio_card] * shape.n_q, np.int32)
+
+
+@dataclasses.dataclass
+class Script:
+    """Per-tick inputs of one session: user codes [T, 8], forced mask/tokens [T, 17]."""
+    user: np.ndarray
+    fmask: np.ndarray
+    forced: np.ndarray
+
+    @property
+    def T(self):
+        return self.user.shape[0]
+
+
+@dataclasses.dataclass
+class Placement:
+    slot: int
+    start: int          # global tick at which the session opens
+    script: Script      # it runs script.T ticks, then closes
+
+
+def device_weights(w_host, device="cuda"):
+    import torch
+    out = {}
+    for k, v in w_host.items():
+        if v.dtype == np.uint16:
+            out[k] = torch.from_numpy(v.view(np.int16)).to(device)
+        else:
+            out[k] = torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device)
+    return out
+
+
+def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=None,
+               oracle_sessions=None):
+    """Run the placements on a GPU engine of B slots with teacher forcing against the
+    oracle; asserts column equality and the logit tolerance every tick.  Returns a dict
+    of statistics."""
+    import torch
+
+    import full_duplex_speech_lockstep_gb300 as pp
+    import oracle
+
+    orc = oracle.Oracle(shape, w_host)
+    eng = pp.Engine(shape, B, w_dev)
+    T_end = max(p.start + p.script.T for p in placements)
+    Vt, Va, nq = shape.text_vocab, shape.audio_card, shape.n_q
+    ld = Vt + nq * Va
+    logits_dev = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+    stats = {"ticks": 0, "max_ratio": 0.0, "gpu_decided": 0, "forced_by_gate": 0}
+    sess = {}
+    for t in range(T_end):
+        for p in placements:
+            if p.start + p.script.T == t:
+                eng.close(p.slot)
+                del sess[p.slot]
+            if p.start == t:
+                eng.open(p.slot)
+                o = (oracle_sessions or {}).get(p.slot)
+                sess[p.slot] = [p, orc.new_session() if o is None else o, initial_column(shape)]
+        prev = np.tile(initial_column(shape), (B, 1))
+        user = np.zeros((B, 8), np.int32)
+        fmask = np.zeros((B, ROWS), np.uint8)
+        forced = np.zeros((B, ROWS), np.int32)
+        expect = {}
+        for slot, (p, os_, pcol) in sess.items():
+            i = t - p.start
+            sc = p.script
+            col, lt, la = orc.step(os_, pcol, sc.user[i], sc.fmask[i], sc.forced[i])
+            expect[slot] = (col, lt, la)
+            prev[slot] = pcol
+            user[slot] = sc.user[i]
+            fm = sc.fmask[i].copy()
+            fm[9:] = 0
+            if not fm[0] and top2_margin(lt) <= TOKEN_MARGIN:
+                fm[0] = 1
+                stats["forced_by_gate"] += 1
+            for k in range(8):
+                if not fm[k + 1] and top2_margin(la[k]) <= TOKEN_MARGIN:
+                    fm[k + 1] = 1
+                    stats["forced_by_gate"] += 1
+            stats["gpu_decided"] += int(9 - fm[:9].sum())
+            fmask[slot] = fm
+            forced[slot, :9] = col[:9]
+            sess[slot][2] = col
+        d = lambda a: torch.from_numpy(a).cuda()
+        colg = eng.step(d(prev), d(user), d(fmask), d(forced), logits=logits_dev if check_logits else None)
+        torch.cuda.synchronize()
+        colg = colg.cpu().numpy()
+        lg = logits_dev.cpu().numpy() if check_logits else None
+        for slot in range(B):
+            if slot not in expect:
+                assert np.all(colg[slot] == -1), (t, slot, colg[slot])
+                continue
+            col, lt, la = expect[slot]
+            assert np.array_equal(colg[slot], col), (t, slot, colg[slot], col)
+            if check_logits:
+                gt = lg[slot, :Vt]
+                r = np.max(np.abs(gt - lt)) / np.std(lt)
+                stats["max_ratio"] = max(stats["max_ratio"], float(r))
+                assert r <= LOGIT_TOL, (t, slot, "text", r)
+                ga = lg[slot, Vt:].reshape(nq, Va)
+                for k in range(nq):
+                    r = np.max(np.abs(ga[k] - la[k])) / np.std(la[k])
+                    stats["max_ratio"] = max(stats["max_ratio"], float(r))
+                    assert r <= LOGIT_TOL, (t, slot, "audio", k, r)
+        stats["ticks"] += 1
+        if report:
+            report(t, stats)
+    st = eng.status()
+    stats["status"] = st
+    eng.close_engine()
+    return stats
+
+
+def greedy_script(shape, T, seed, stream=100):
+    """Free-running greedy session: uniform user codes, nothing forced."""
+    import synth
+    user = synth.uniform_i32(T * 8, seed, stream, 0, shape.audio_card).reshape(T, 8)
+    return Script(user, np.zeros((T, ROWS), np.uint8), np.zeros((T, ROWS), np.int32))

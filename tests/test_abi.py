@@ -1,0 +1,78 @@
+"""The C ABI library loads and exports every function include/pp.h declares; host-side
+configuration checks (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import full_duplex_speech_lockstep_gb300 as pp
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pp_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    lib = pp.lib()
+    declared = _declared()
+    assert declared == sorted(pp.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_weight_enum_matches_header():
+    text = open(os.path.join(ROOT, "include", "pp.h")).read()
+    names = re.findall(r"\bPP_W_([A-Z_]+)\s*[,=]", text)
+    names = [n.lower() for n in names if n != "COUNT"]
+    # header name -> binding name: matrices carry a "w" prefix in the binding
+    rename = {"qkv": "wqkv", "o": "wo", "gu": "wgu", "down": "wdown", "text": "wtext",
+              "dep_qkv": "dep_wqkv", "dep_o": "dep_wo", "dep_gu": "dep_wgu",
+              "dep_down": "dep_wdown"}
+    assert [rename.get(n, n) for n in names] == pp.WEIGHT_NAMES
+    assert pp.WEIGHT_NAMES == synth.weight_names()
+
+
+def test_weight_shapes_match_generator():
+    for shape in [synth.TINY, synth.SMALL, synth.FULL]:
+        cfg = pp.make_config(shape, 4)
+        specs = {n: (shp, dt) for n, shp, dt, _ in synth.weight_specs(shape)}
+        for i, name in enumerate(pp.WEIGHT_NAMES):
+            dims, f32 = pp.pp_weight_shape(cfg, i)
+            assert dims == specs[name][0], name
+            assert f32 == (specs[name][1] == "f32"), name
+
+
+def test_workspace_size_and_config_validation():
+    full = pp.pp_workspace_bytes(pp.make_config(synth.FULL, 64))
+    ring = 32 * 64 * 2 * 32 * 3000 * 128 * 2
+    assert ring <= full < ring + (1 << 30)
+    assert pp.pp_workspace_bytes(pp.make_config(synth.FULL, 1)) < full
+    bad = pp.make_config(synth.TINY, 0)
+    with pytest.raises(pp.PPError):
+        pp.pp_workspace_bytes(bad)
+    bad = pp.make_config(synth.TINY, 65)
+    with pytest.raises(pp.PPError):
+        pp.pp_workspace_bytes(bad)
+    import dataclasses
+    bad = pp.make_config(dataclasses.replace(synth.TINY, n_heads=3), 1)
+    with pytest.raises(pp.PPError):
+        pp.pp_workspace_bytes(bad)
+    with pytest.raises(pp.PPError):
+        pp.pp_weight_shape(pp.make_config(synth.TINY, 1), pp.PP_W_COUNT)
+
+
+def test_create_rejects_bad_arguments_without_touching_the_gpu():
+    cfg = pp.make_config(synth.TINY, 1)
+    lib = pp.lib()
+    h = ctypes.c_void_p()
+    w = pp.pp_weights()
+    # null weights / workspace are rejected before any CUDA call
+    assert lib.pp_create(ctypes.byref(cfg), ctypes.byref(w), None, 0, ctypes.byref(h)) == pp.PP_EINVAL
+    assert lib.pp_session_open(None, 0) == pp.PP_EINVAL
+    assert lib.pp_step(None, None, None, None, None, None, None, None) == pp.PP_EINVAL
