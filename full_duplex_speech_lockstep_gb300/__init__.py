@@ -52,7 +52,9 @@ class pp_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ["d_model", "n_layers", "n_heads", "ffn", "text_vocab", "audio_card", "n_q",
                  "dep_d", "dep_layers", "dep_heads", "dep_ffn", "window", "max_batch"]] + [
-        ("eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
+        ("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+PP_FLAG_CUDA_CORE_GEMM = 0x1
 
 
 class pp_weights(ctypes.Structure):
@@ -109,12 +111,12 @@ def _check(fn, rc):
     return rc
 
 
-def make_config(shape, max_batch):
+def make_config(shape, max_batch, flags=0):
     """pp_config from an object with the model's dimensions (by attribute name)."""
     return pp_config(shape.d, shape.n_layers, shape.n_heads, shape.ffn, shape.text_vocab,
                      shape.audio_card, shape.n_q, shape.dep_d, shape.dep_layers,
                      shape.dep_heads, shape.dep_ffn, shape.window, int(max_batch),
-                     float(shape.eps), float(shape.rope_base))
+                     float(shape.eps), float(shape.rope_base), int(flags))
 
 
 # ---- the C ABI, one wrapper per entry point -------------------------------------------
@@ -205,12 +207,12 @@ def pp_profile_step(h, prev_column, user_codes, force_mask, forced_tokens, colum
 class Engine:
     """One engine over torch-owned device memory (weights dict + workspace)."""
 
-    def __init__(self, shape, max_batch, weights, device="cuda"):
+    def __init__(self, shape, max_batch, weights, device="cuda", flags=0):
         import torch
         self.torch = torch
         self.shape = shape
         self.B = int(max_batch)
-        self.cfg = make_config(shape, max_batch)
+        self.cfg = make_config(shape, max_batch, flags)
         self.weights = weights
         ptrs = []
         for i, name in enumerate(WEIGHT_NAMES):

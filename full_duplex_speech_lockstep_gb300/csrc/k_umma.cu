@@ -289,8 +289,11 @@ __global__ void __launch_bounds__(128, 2)
   // ---- final epilogue ------------------------------------------------------------------
   if (a.epi == EPI_SILU) {
     float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
-    if (r >= 64)
-      for (int b = 0; b < B; ++b) xch[(r - 64) * Bp + b] = acc[b];
+    if (r >= 64) {
+#pragma unroll
+      for (int b = 0; b < N / 2; ++b)
+        if (b < B) xch[(r - 64) * Bp + b] = acc[b];
+    }
     __syncthreads();
     if (r < 64 && row_ok) {
 #pragma unroll

@@ -28,10 +28,22 @@ struct Prof {
   }
 };
 
+// One family of tensor-core contractions (one stacked weight tensor).
+struct Mm {
+  CUtensorMap mapA;    // stacked weights [rows_total, K] bf16, box 64 k x 64 rows
+  CUtensorMap mapB;    // activation operand [2*Bp, K] bf16, box 64 k x 2*Bp rows
+  int M = 0, K = 0, kblocks = 0, splits = 1, m_tiles = 0, pair = 0;
+};
+
+enum MmKind { MM_QKV, MM_O, MM_GU, MM_DOWN, MM_TEXT, MM_DIN, MM_DQKV, MM_DO, MM_DGU, MM_DDOWN,
+              MM_DHEAD, MM_COUNT };
+
 struct pp_engine {
   pp_config cfg;
   Dims D;
   Buffers buf;
+  bool tensor = true;
+  Mm mm[MM_COUNT];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -66,6 +78,7 @@ bool config_ok(const pp_config* c) {
 
 Dims make_dims(const pp_config* c) {
   Dims D;
+  D.Bp = (c->max_batch + 7) / 8 * 8;
   D.d = c->d_model; D.L = c->n_layers; D.H = c->n_heads; D.Dh = c->d_model / c->n_heads;
   D.F = c->ffn; D.Vt = c->text_vocab; D.Va = c->audio_card; D.nq = c->n_q;
   D.dd = c->dep_d; D.Ld = c->dep_layers; D.Hd = c->dep_heads; D.Dhd = c->dep_d / c->dep_heads;
@@ -123,6 +136,16 @@ size_t carve(const Dims& D, char* base, Buffers* b) {
   b->dkv = cv.take<float>(B * D.Ld * D.nq * 2 * D.dd);
   b->dout = cv.take<float>(B * D.dd);
   b->dh = cv.take<float>(B * D.Fd);
+  const size_t R = 2 * (size_t)D.Bp;
+  b->op_d = cv.take<uint16_t>(R * D.d);
+  b->op_o = cv.take<uint16_t>(R * D.d);
+  b->op_f = cv.take<uint16_t>(R * D.F);
+  b->op_z = cv.take<uint16_t>(R * D.d);
+  b->op_dd = cv.take<uint16_t>(R * D.dd);
+  b->op_do = cv.take<uint16_t>(R * D.dd);
+  b->op_fd = cv.take<uint16_t>(R * D.Fd);
+  b->tile_count = cv.take<uint32_t>(kMaxTiles);
+  b->partial = cv.take<float>((size_t)kMaxUnits * 128 * B);
   return (cv.off + 255) & ~(size_t)255;
 }
 
@@ -132,19 +155,194 @@ size_t carve(const Dims& D, char* base, Buffers* b) {
     if (err_ != cudaSuccess) return err_; \
   } while (0)
 
-// The whole tick, in stream order.  With prof != nullptr a timing event is recorded
-// before every launch (and once at the end).
+
+// ---- tensor maps and contraction plans ------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, k] matrix, 64-element (128-byte) inner box with
+// the 128-byte swizzle; out-of-range rows and columns read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[2] = {k, rows};
+  cuuint64_t gstride[1] = {k * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K-splits per M-tile: a function of the matrix shape and the device's CTA slots only.
+int choose_splits(int m_tiles, int kblocks, int slots) {
+  int best = 1;
+  double best_t = 1e300;
+  for (int sp = 1; sp <= kblocks && m_tiles * sp <= kMaxUnits; ++sp) {
+    const int units = m_tiles * sp;
+    const int waves = (units + slots - 1) / slots;
+    const double t = waves * ((double)((kblocks + sp - 1) / sp) + 3.0);
+    if (t < best_t - 1e-9) { best_t = t; best = sp; }
+  }
+  return best;
+}
+
+bool plan_mm(Mm* g, const void* w, int rows_total, int M, int K, int pair, const uint16_t* op,
+             int Bp, int slots) {
+  g->M = M;
+  g->K = K;
+  g->pair = pair;
+  g->kblocks = (K + 63) / 64;
+  g->m_tiles = pair ? (pair + 63) / 64 : (M + 127) / 128;
+  if (g->m_tiles > kMaxTiles) return false;
+  g->splits = choose_splits(g->m_tiles, g->kblocks, slots);
+  return make_map(&g->mapA, w, (uint64_t)rows_total, (uint64_t)K, 64) &&
+         make_map(&g->mapB, op, (uint64_t)2 * Bp, (uint64_t)K, 2 * Bp);
+}
+
+bool plan_all(pp_engine* e, int slots) {
+  const Dims& D = e->D;
+  const Buffers& b = e->buf;
+  const int Bp = D.Bp;
+  bool ok = true;
+  ok &= plan_mm(&e->mm[MM_QKV], b.wqkv, D.L * 3 * D.d, 3 * D.d, D.d, 0, b.op_d, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_O], b.wo, D.L * D.d, D.d, D.d, 0, b.op_o, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_dd, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_do, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_dd, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DDOWN], b.dep_wdown, D.Ld * D.dd, D.dd, D.Fd, 0, b.op_fd, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_DHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_dd, Bp, slots);
+  return ok;
+}
+
+// One tensor-core contraction launch: matrix `row0` rows into its stacked tensor.
+cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, int epi, float* Y,
+                      int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s) {
+  UmmaArgs a{};
+  a.M = g.M;
+  a.pair_rows = g.pair;
+  a.row0 = row0;
+  a.kblocks = g.kblocks;
+  a.splits = g.splits;
+  a.m_tiles = g.m_tiles;
+  a.B = D.B;
+  a.N = 2 * D.Bp;
+  a.epi = epi;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.emb = emb;
+  a.tok = b.tok;
+  a.op_out = op_out;
+  a.ld_op = ld_op;
+  a.Bp_out = D.Bp;
+  a.partial = b.partial;
+  a.counter = b.tile_count;
+  a.status = b.status;
+  return launch_umma(a, g.mapA, g.mapB, s);
+}
+
 #define MARK(k)                                 \
   do {                                          \
     if (prof) PP_TRY(prof->mark((k), s));       \
   } while (0)
 
-cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* prof) {
+// The tick with every weight contraction on the tensor cores.
+cudaError_t enqueue_tick_tensor(const pp_engine* e, cudaStream_t s, Prof* prof) {
+  const Dims& D = e->D;
+  const Buffers& b = e->buf;
+  const Mm* mm = e->mm;
   MARK(PP_K_BEGIN);
   PP_TRY(launch_begin(D, b, s));
   for (int l = 0; l < D.L; ++l) {
     MARK(PP_K_NORM);
-    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, b.xn, D.d, s));
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, nullptr, 0, b.op_d, s));
+    MARK(PP_K_QKV);
+    PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_STORE, b.qkv, 3 * D.d, nullptr, nullptr, 0, s));
+    MARK(PP_K_ROPE_RING);
+    PP_TRY(launch_rope_ring(D, b, l, s));
+    MARK(PP_K_ATTN);
+    PP_TRY(launch_attn(D, b, l, true, s));
+    MARK(PP_K_OPROJ);
+    PP_TRY(mm_launch(D, b, mm[MM_O], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s));
+    MARK(PP_K_NORM);
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.mlp_alpha + (size_t)l * D.d, D.d, nullptr, 0, b.op_d, s));
+    MARK(PP_K_GATEUP);
+    PP_TRY(mm_launch(D, b, mm[MM_GU], l * 2 * D.F, EPI_SILU, nullptr, 0, nullptr, b.op_f, D.F, s));
+    MARK(PP_K_DOWN);
+    PP_TRY(mm_launch(D, b, mm[MM_DOWN], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s));
+  }
+  MARK(PP_K_TEXT_HEAD);
+  PP_TRY(launch_rmsnorm(D, b.x, D.d, b.out_alpha, D.d, nullptr, 0, b.op_z, s));
+  MARK(PP_K_TEXT_HEAD);
+  PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s));
+  MARK(PP_K_TEXT_HEAD);
+  PP_TRY(launch_text_argmax(D, b, s));
+  for (int k = 0; k < D.nq; ++k) {
+    const uint16_t* emb =
+        (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(mm_launch(D, b, mm[MM_DIN], k * D.dd, EPI_EMB, b.y, D.dd, emb, nullptr, 0, s));
+    for (int j = 0; j < D.Ld; ++j) {
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
+                            b.op_dd, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(mm_launch(D, b, mm[MM_DQKV], j * 3 * D.dd, EPI_STORE, b.dqkv, 3 * D.dd, nullptr,
+                       nullptr, 0, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(launch_dep_attn(D, b, k, j, true, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(mm_launch(D, b, mm[MM_DO], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
+                            b.op_dd, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(mm_launch(D, b, mm[MM_DGU], j * 2 * D.Fd, EPI_SILU, nullptr, 0, nullptr, b.op_fd,
+                       D.Fd, s));
+      MARK(PP_K_DEPFORMER);
+      PP_TRY(mm_launch(D, b, mm[MM_DDOWN], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
+    }
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, nullptr, 0, b.op_dd, s));
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(mm_launch(D, b, mm[MM_DHEAD], k * D.Va, EPI_STORE, b.logits + D.Vt + (size_t)k * D.Va,
+                     D.logits_ld, nullptr, nullptr, 0, s));
+    MARK(PP_K_DEPFORMER);
+    PP_TRY(launch_dep_argmax(D, b, k, s));
+  }
+  MARK(PP_K_FINISH);
+  PP_TRY(launch_finish(D, b, s));
+  MARK(PP_K_COUNT);
+  return cudaSuccess;
+}
+
+// The tick with the CUDA-core contractions.  With prof != nullptr a timing event is
+// recorded before every launch (and once at the end).
+cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Prof* prof) {
+  MARK(PP_K_BEGIN);
+  PP_TRY(launch_begin(D, b, s));
+  for (int l = 0; l < D.L; ++l) {
+    MARK(PP_K_NORM);
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, b.xn, D.d, nullptr, s));
     GemvArgs a{};
     a.W = b.wqkv + (size_t)l * 3 * D.d * D.d; a.M = 3 * D.d; a.K = D.d;
     a.X = b.xn; a.ldx = D.d; a.Y = b.qkv; a.ldy = 3 * D.d; a.epi = EPI_STORE;
@@ -153,14 +351,14 @@ cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* 
     MARK(PP_K_ROPE_RING);
     PP_TRY(launch_rope_ring(D, b, l, s));
     MARK(PP_K_ATTN);
-    PP_TRY(launch_attn(D, b, l, s));
+    PP_TRY(launch_attn(D, b, l, false, s));
     a = GemvArgs{};
     a.W = b.wo + (size_t)l * D.d * D.d; a.M = D.d; a.K = D.d;
     a.X = b.o; a.ldx = D.d; a.Y = b.x; a.ldy = D.d; a.epi = EPI_ADD;
     MARK(PP_K_OPROJ);
     PP_TRY(launch_gemv(D, a, s));
     MARK(PP_K_NORM);
-    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.mlp_alpha + (size_t)l * D.d, D.d, b.xn, D.d, s));
+    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.mlp_alpha + (size_t)l * D.d, D.d, b.xn, D.d, nullptr, s));
     a = GemvArgs{};
     a.W = b.wgu + (size_t)l * 2 * D.F * D.d; a.M = D.F; a.K = D.d;
     a.X = b.xn; a.ldx = D.d; a.Y = b.hmlp; a.ldy = D.F; a.epi = EPI_SILU;
@@ -173,7 +371,7 @@ cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* 
     PP_TRY(launch_gemv(D, a, s));
   }
   MARK(PP_K_TEXT_HEAD);
-  PP_TRY(launch_rmsnorm(D, b.x, D.d, b.out_alpha, D.d, b.z, D.d, s));
+  PP_TRY(launch_rmsnorm(D, b.x, D.d, b.out_alpha, D.d, b.z, D.d, nullptr, s));
   {
     GemvArgs a{};
     a.W = b.wtext; a.M = D.Vt; a.K = D.d;
@@ -193,21 +391,21 @@ cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* 
     PP_TRY(launch_gemv(D, a, s));
     for (int j = 0; j < D.Ld; ++j) {
       MARK(PP_K_DEPFORMER);
-    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, s));
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, nullptr, s));
       a = GemvArgs{};
       a.W = b.dep_wqkv + (size_t)j * 3 * D.dd * D.dd; a.M = 3 * D.dd; a.K = D.dd;
       a.X = b.yn; a.ldx = D.dd; a.Y = b.dqkv; a.ldy = 3 * D.dd; a.epi = EPI_STORE;
       MARK(PP_K_DEPFORMER);
     PP_TRY(launch_gemv(D, a, s));
       MARK(PP_K_DEPFORMER);
-    PP_TRY(launch_dep_attn(D, b, k, j, s));
+    PP_TRY(launch_dep_attn(D, b, k, j, false, s));
       a = GemvArgs{};
       a.W = b.dep_wo + (size_t)j * D.dd * D.dd; a.M = D.dd; a.K = D.dd;
       a.X = b.dout; a.ldx = D.dd; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_ADD;
       MARK(PP_K_DEPFORMER);
     PP_TRY(launch_gemv(D, a, s));
       MARK(PP_K_DEPFORMER);
-    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, s));
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, nullptr, s));
       a = GemvArgs{};
       a.W = b.dep_wgu + (size_t)j * 2 * D.Fd * D.dd; a.M = D.Fd; a.K = D.dd;
       a.X = b.yn; a.ldx = D.dd; a.Y = b.dh; a.ldy = D.Fd; a.epi = EPI_SILU;
@@ -220,7 +418,7 @@ cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* 
     PP_TRY(launch_gemv(D, a, s));
     }
     MARK(PP_K_DEPFORMER);
-    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, b.yn, D.dd, s));
+    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, b.yn, D.dd, nullptr, s));
     a = GemvArgs{};
     a.W = b.dep_heads + (size_t)k * D.Va * D.dd; a.M = D.Va; a.K = D.dd;
     a.X = b.yn; a.ldx = D.dd; a.Y = b.logits + D.Vt + (size_t)k * D.Va; a.ldy = D.logits_ld;
@@ -234,6 +432,10 @@ cudaError_t enqueue_tick(const Dims& D, const Buffers& b, cudaStream_t s, Prof* 
   PP_TRY(launch_finish(D, b, s));
   MARK(PP_K_COUNT);   // end marker
   return cudaSuccess;
+}
+
+cudaError_t enqueue_tick(const pp_engine* e, cudaStream_t s, Prof* prof) {
+  return e->tensor ? enqueue_tick_tensor(e, s, prof) : enqueue_tick_cc(e->D, e->buf, s, prof);
 }
 
 int weight_dims(const pp_config* c, int which, int64_t d[4], int* nd, int* f32) {
@@ -330,16 +532,30 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   e->pos.assign(D.B, 0);
   e->open.assign(D.B, 0);
 
+  e->tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
   cudaError_t err = cudaSuccess;
   // zero the small state (positions, liveness, control, status, attention counters)
   char* small_lo = reinterpret_cast<char*>(b.pos);
   char* small_hi = reinterpret_cast<char*>(b.in_col);
   err = cudaMemset(small_lo, 0, (size_t)(small_hi - small_lo));
+  if (err == cudaSuccess) {   // operands (their padding rows stay zero) and split-K tickets
+    char* op_lo = reinterpret_cast<char*>(b.op_d);
+    char* op_hi = reinterpret_cast<char*>(b.partial);
+    err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
+  }
+  if (err == cudaSuccess && e->tensor) {
+    int dev = 0, nsm = 0;
+    err = cudaGetDevice(&dev);
+    if (err == cudaSuccess)
+      err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = umma_setup(2 * D.Bp);
+    if (err == cudaSuccess && !plan_all(e, 2 * nsm)) err = cudaErrorInvalidValue;
+  }
   if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking);
   if (err == cudaSuccess)
     err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
   if (err == cudaSuccess) {
-    cudaError_t le = enqueue_tick(e->D, e->buf, e->cap_stream, nullptr);
+    cudaError_t le = enqueue_tick(e, e->cap_stream, nullptr);
     err = cudaStreamEndCapture(e->cap_stream, &e->graph);
     if (le != cudaSuccess) err = le;
   }
@@ -478,7 +694,7 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
   if (!e->prof_exec) {   // capture the profiling graph on first use
     cudaError_t err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
     if (err == cudaSuccess) {
-      cudaError_t le = enqueue_tick(e->D, e->buf, e->cap_stream, &e->prof);
+      cudaError_t le = enqueue_tick(e, e->cap_stream, &e->prof);
       err = cudaStreamEndCapture(e->cap_stream, &e->prof_graph);
       if (le != cudaSuccess) err = le;
     }

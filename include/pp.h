@@ -71,7 +71,13 @@ typedef struct {
   int32_t max_batch;     /* slots, 1..64 */
   float eps;             /* RMSNorm epsilon (inside the square root) */
   float rope_base;       /* RoPE base (10000) */
+  int32_t flags;         /* PP_FLAG_* bits; 0 = default */
 } pp_config;
+
+/* Weight contractions on CUDA cores (fp32 activations) instead of the default
+ * tcgen05 tensor-core path (split-bf16 activations).  The two paths round
+ * differently, so a session's bits are reproducible within one path only. */
+#define PP_FLAG_CUDA_CORE_GEMM 0x1
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */

@@ -60,7 +60,7 @@ def device_weights(w_host, device="cuda"):
 
 
 def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=None,
-               oracle_sessions=None):
+               oracle_sessions=None, flags=0):
     """Run the placements on a GPU engine of B slots with teacher forcing against the
     oracle; asserts column equality and the logit tolerance every tick.  Returns a dict
     of statistics."""
@@ -70,7 +70,7 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
     import oracle
 
     orc = oracle.Oracle(shape, w_host)
-    eng = pp.Engine(shape, B, w_dev)
+    eng = pp.Engine(shape, B, w_dev, flags=flags)
     T_end = max(p.start + p.script.T for p in placements)
     Vt, Va, nq = shape.text_vocab, shape.audio_card, shape.n_q
     ld = Vt + nq * Va

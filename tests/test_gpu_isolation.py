@@ -1,0 +1,92 @@
+"""Batch isolation (GPU): every session's columns and logits in a batched engine are
+bit-identical to the same session run alone in a one-slot engine, whichever other
+sessions join, leave or recycle slots around it."""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from synth import schedules
+from harness import ROWS, device_weights, initial_column
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(eng, B, shape, sessions, T_end, want_logits=True):
+    """Free-running greedy run of `sessions` [(slot, start, user, fmask, forced)] on
+    `eng`; returns per-session (columns [T,17], logits [T, ld])."""
+    import torch
+    ld = shape.text_vocab + shape.n_q * shape.audio_card
+    logits = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+    out = {i: ([], []) for i in range(len(sessions))}
+    prev = {}
+    live = {}
+    for t in range(T_end):
+        for i, (slot, start, user, fm, fo) in enumerate(sessions):
+            if start + user.shape[0] == t:
+                eng.close(slot)
+                del live[slot]
+        for i, (slot, start, user, fm, fo) in enumerate(sessions):
+            if start == t:
+                eng.open(slot)
+                live[slot] = i
+                prev[i] = initial_column(shape)
+        if not live:
+            continue
+        P = np.tile(initial_column(shape), (B, 1))
+        U = np.zeros((B, 8), np.int32)
+        FM = np.zeros((B, ROWS), np.uint8)
+        FO = np.zeros((B, ROWS), np.int32)
+        for slot, i in live.items():
+            _, start, user, fm, fo = sessions[i]
+            k = t - start
+            P[slot], U[slot], FM[slot], FO[slot] = prev[i], user[k], fm[k], fo[k]
+        d = lambda a: torch.from_numpy(a).cuda()
+        col = eng.step(d(P), d(U), d(FM), d(FO), logits=logits if want_logits else None)
+        col = col.cpu().numpy()
+        lg = logits.cpu().numpy() if want_logits else None
+        for slot, i in live.items():
+            prev[i] = col[slot].copy()
+            out[i][0].append(col[slot].copy())
+            if want_logits:
+                out[i][1].append(lg[slot].copy())
+    return out
+
+
+def _check_isolation(shape, B, sessions, T_end, w_dev):
+    import full_duplex_speech_lockstep_gb300 as pp
+    eng = pp.Engine(shape, B, w_dev)
+    batched = _run(eng, B, shape, sessions, T_end)
+    assert eng.status() == 0
+    eng.close_engine()
+    for i, (slot, start, user, fm, fo) in enumerate(sessions):
+        e1 = pp.Engine(shape, 1, w_dev)
+        alone = _run(e1, 1, shape, [(0, 0, user, fm, fo)], user.shape[0])
+        e1.close_engine()
+        bc, bl = np.array(batched[i][0]), np.array(batched[i][1])
+        ac, al = np.array(alone[0][0]), np.array(alone[0][1])
+        assert np.array_equal(bc, ac), ("columns differ", i, slot, start)
+        assert np.array_equal(bl.view(np.uint32), al.view(np.uint32)), ("logits differ", i)
+
+
+def test_elastic_isolation_small():
+    """B=12 (two operand groups of 8) with joins, leaves and recycled slots."""
+    s = synth.SMALL
+    w = synth.make_weights_host(s, 11, alpha="random")
+    sessions = schedules.elastic_schedule(s, 3, n_slots=12, T=120, initial=6, mean_gap=6,
+                                          prefill=(8, 30))
+    assert len(sessions) > 12
+    _check_isolation(s, 12, sessions, 120, device_weights(w))
+
+
+def test_isolation_across_engine_sizes():
+    """The same session in a 64-slot engine (N = 128 operand rows) next to 63 others,
+    and alone (N = 16): bit-identical."""
+    s = synth.TINY
+    w = synth.make_weights_host(s, 12)
+    sess = []
+    for i in range(64):
+        user, fm, fo = schedules.prefill_session(s, 100 + i, T=20, voice=3, persona=4)
+        sess.append((i, i % 5, user, fm, fo))
+    _check_isolation(s, 64, sess[:1] + sess[1:], 25, device_weights(w))

@@ -21,6 +21,7 @@ def test_tiny_config_greedy_96_ticks():
     s = synth.TINY
     w = synth.make_weights_host(s, 0)
     st = run_parity(s, 1, w, device_weights(w), [Placement(0, 0, greedy_script(s, 96, 0))])
+    print("parity tiny", st)
     assert st["ticks"] == 96 and st["status"] == 0
     assert st["gpu_decided"] > 500
 
@@ -36,6 +37,7 @@ def test_small_ragged_batch_staggered_recycled():
           Placement(4, 17, greedy_script(s, 50, 4)),
           Placement(3, 75, greedy_script(s, 55, 5))]    # slot 3 recycled
     st = run_parity(s, 5, w, device_weights(w), pl)
+    print("parity small", st)
     assert st["status"] == 0
 
 

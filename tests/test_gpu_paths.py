@@ -1,0 +1,48 @@
+"""The two contraction paths (tcgen05 tensor cores with split-bf16 activations, CUDA
+cores with fp32 activations) against each other and against the oracle (GPU)."""
+import numpy as np
+import pytest
+
+import synth
+from harness import Placement, device_weights, greedy_script, run_parity
+
+pytestmark = pytest.mark.gpu
+
+
+def test_cuda_core_path_parity():
+    """The CUDA-core contraction path passes the same oracle gate."""
+    import full_duplex_speech_lockstep_gb300 as pp
+    s = synth.TINY
+    w = synth.make_weights_host(s, 21, alpha="random")
+    st = run_parity(s, 3, w, device_weights(w),
+                    [Placement(0, 0, greedy_script(s, 40, 1)), Placement(2, 5, greedy_script(s, 30, 2))],
+                    flags=pp.PP_FLAG_CUDA_CORE_GEMM)
+    assert st["status"] == 0
+
+
+@pytest.mark.parametrize("B", [1, 9, 64])
+def test_paths_agree(B):
+    """One tick from the same state: both paths' logits agree to fp32-level error."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    s = synth.SMALL
+    w = device_weights(synth.make_weights_host(s, 22, alpha="random"))
+    ld = s.text_vocab + s.n_q * s.audio_card
+    outs = []
+    for flags in [0, pp.PP_FLAG_CUDA_CORE_GEMM]:
+        e = pp.Engine(s, B, w, flags=flags)
+        for b in range(B):
+            e.open(b)
+        prev = torch.from_numpy(np.tile(np.array([s.text_vocab] + [s.audio_card] * 16, np.int32), (B, 1))).cuda()
+        user = torch.from_numpy(synth.uniform_i32(B * 8, 3, 3, 0, 2048).reshape(B, 8)).cuda()
+        lg = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+        fm = torch.ones((B, 17), dtype=torch.uint8, device="cuda")
+        fo = torch.zeros((B, 17), dtype=torch.int32, device="cuda")
+        e.step(prev, user, fm, fo, logits=lg)
+        torch.cuda.synchronize()
+        outs.append(lg.cpu().numpy())
+        assert e.status() == 0
+        e.close_engine()
+    a, b = outs
+    scale = np.std(a)
+    assert np.max(np.abs(a - b)) <= 1e-3 * scale
