@@ -33,6 +33,14 @@ UNIT = "session-frames/s"
 SEED = 5
 HBM_NOMINAL_GBS = 8000.0
 
+# DRAM traffic of the attention kernel from one ncu capture (profiles/
+# k_attn_b8_fullshape_2layers.md): dram__bytes_read + dram__bytes_write of one launch at
+# B=8 with a full 3000-position ring, per (slot, valid position).  Traffic grows in
+# proportion to the slots, so a full launch's traffic is this times slots x positions.
+# Valid only while k_attn.cu is the source that was captured (its hash below).
+ATTN_TRAFFIC = {"bytes_per_slot_position": (393.383168e6 + 4.116992e6) / (8 * 3000),
+                "source_sha256_16": "18f863747c5a8737"}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -48,6 +56,10 @@ def parse():
     ap.add_argument("--cpu-ticks", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="full", choices=["tiny", "small", "full"])
+    ap.add_argument("--engine-flags", type=int, default=0, help="pp_config.flags (PP_FLAG_*)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="temporal layers (0 = the shape's own); fewer layers give a small "
+                         "case with full-size kernels for profiling")
     return ap.parse_args()
 
 
@@ -279,12 +291,15 @@ def main():
     import full_duplex_speech_lockstep_gb300 as pp
     import synth
     shape = synth.PRESETS[a.shape]
+    if a.layers:
+        import dataclasses
+        shape = dataclasses.replace(shape, n_layers=a.layers)
     B = a.batch
     pos = a.pos
     props = torch.cuda.get_device_properties(local)
 
     w_dev = synth.make_weights_device(shape, SEED)
-    eng = pp.Engine(shape, B, w_dev)
+    eng = pp.Engine(shape, B, w_dev, flags=a.engine_flags)
     fill_rings(eng, shape, B, pos)
     kernels_per_tick = eng.kernel_count()
 
@@ -330,15 +345,20 @@ def main():
                 "ms_per_launch": (kind_ms[i] / kind_n[i]) if kind_n[i] else 0.0}
             for i, k in enumerate(pp.KERNEL_KINDS)}
     ia = pp.KERNEL_KINDS.index("attn")
-    attn_ms = kind_ms[ia] / max(1, kind_n[ia])
+    attn_ms = kind_ms[ia] / kind_n[ia] if kind_n[ia] else float("nan")
     # algorithmic bytes of one attention launch (one layer): K and V of every valid
     # ring position of every head, plus q in and o out (fp32)
     n_prof = min(pos + a.warmup + a.steps + a.profile_steps, shape.window)
     attn_bytes = B * n_prof * 2 * shape.d * 2 + 2 * B * shape.d * 4
-    attn_gbs = attn_bytes / (attn_ms / 1000.0) / 1e9
+    attn_gbs = attn_bytes / (attn_ms / 1000.0) / 1e9 if kind_n[ia] else None
+    traffic = None
+    import hashlib
+    src = os.path.join(ROOT, "full_duplex_speech_lockstep_gb300", "csrc", "k_attn.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == ATTN_TRAFFIC["source_sha256_16"]:
+        traffic = ATTN_TRAFFIC["bytes_per_slot_position"] * B * n_prof
     roofline = {"kernel": "k_attn (split-K ring attention)", "bound": "hbm",
                 "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
-                "frac": attn_gbs / hbm_peak, "traffic": None,
+                "frac": attn_gbs / hbm_peak if attn_gbs else None, "traffic": traffic,
                 "peak_source": peak_src, "bytes_per_launch": attn_bytes,
                 "ms_per_launch": attn_ms}
 
@@ -369,7 +389,7 @@ def main():
     # -- B=1 latency line (full shape, fresh session) ---------------------------------------
     b1 = None
     if a.b1_steps > 0:
-        e1 = pp.Engine(shape, 1, w_dev)
+        e1 = pp.Engine(shape, 1, w_dev, flags=a.engine_flags)
         e1.open(0)
         ms1, per1 = time_ticks(e1, 1, shape, a.b1_steps, max(3, a.warmup), 700)
         b1 = {"session_frames_s": a.b1_steps / (ms1 / 1000.0),

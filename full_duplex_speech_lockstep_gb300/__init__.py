@@ -39,7 +39,8 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
-                "text_head", "depformer", "finish"]
+                "text_head", "dep_inproj", "dep_norm", "dep_qkv", "dep_attn", "dep_oproj",
+                "dep_gateup", "dep_down", "dep_head", "finish"]
 
 
 class PPError(RuntimeError):
@@ -55,6 +56,7 @@ class pp_config(ctypes.Structure):
         ("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", ctypes.c_int32)]
 
 PP_FLAG_CUDA_CORE_GEMM = 0x1
+PP_FLAG_PDL = 0x2
 
 
 class pp_weights(ctypes.Structure):

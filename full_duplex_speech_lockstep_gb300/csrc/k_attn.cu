@@ -39,6 +39,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
 
 template <int DH>
 __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int layer, bool op) {
+  pdl_wait_and_trigger();
   constexpr int PIECES = DH / 8;        // 16-byte pieces per K/V row
   constexpr int LOADS = PIECES / 4;     // pieces per lane (4 lanes per key)
   constexpr int ITER = 32 / 8;          // 8 keys per warp iteration, 32 keys per warp
@@ -207,9 +208,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
 cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s) {
   const dim3 grid(D.nc_max, D.H, D.B);
   switch (D.Dh) {
-    case 32: k_attn<32><<<grid, kAttnWarps * 32, 0, s>>>(D, b, layer, op); break;
-    case 64: k_attn<64><<<grid, kAttnWarps * 32, 0, s>>>(D, b, layer, op); break;
-    case 128: k_attn<128><<<grid, kAttnWarps * 32, 0, s>>>(D, b, layer, op); break;
+    case 32: { cudaError_t e_ = launch_k(k_attn<32>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
+    case 64: { cudaError_t e_ = launch_k(k_attn<64>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
+    case 128: { cudaError_t e_ = launch_k(k_attn<128>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

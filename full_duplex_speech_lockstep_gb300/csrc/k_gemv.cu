@@ -34,6 +34,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
 
 template <int NB, int EPI>
 __global__ void __launch_bounds__(256) k_gemv(Dims D, GemvArgs a) {
+  pdl_wait_and_trigger();
   constexpr int R = (EPI == EPI_SILU) ? 2 : 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
@@ -96,10 +97,10 @@ template <int NB>
 cudaError_t gemv_nb(const Dims& D, const GemvArgs& a, cudaStream_t s) {
   const dim3 grid((a.M + 7) / 8);
   switch (a.epi) {
-    case EPI_STORE: k_gemv<NB, EPI_STORE><<<grid, 256, 0, s>>>(D, a); break;
-    case EPI_ADD: k_gemv<NB, EPI_ADD><<<grid, 256, 0, s>>>(D, a); break;
-    case EPI_SILU: k_gemv<NB, EPI_SILU><<<grid, 256, 0, s>>>(D, a); break;
-    case EPI_EMB: k_gemv<NB, EPI_EMB><<<grid, 256, 0, s>>>(D, a); break;
+    case EPI_STORE: { cudaError_t e_ = launch_k(k_gemv<NB, EPI_STORE>, dim3(grid), dim3(256), 0, s, 1, D, a); if (e_ != cudaSuccess) return e_; } break;
+    case EPI_ADD: { cudaError_t e_ = launch_k(k_gemv<NB, EPI_ADD>, dim3(grid), dim3(256), 0, s, 1, D, a); if (e_ != cudaSuccess) return e_; } break;
+    case EPI_SILU: { cudaError_t e_ = launch_k(k_gemv<NB, EPI_SILU>, dim3(grid), dim3(256), 0, s, 1, D, a); if (e_ != cudaSuccess) return e_; } break;
+    case EPI_EMB: { cudaError_t e_ = launch_k(k_gemv<NB, EPI_EMB>, dim3(grid), dim3(256), 0, s, 1, D, a); if (e_ != cudaSuccess) return e_; } break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

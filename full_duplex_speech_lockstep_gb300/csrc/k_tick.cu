@@ -52,6 +52,7 @@ __device__ __forceinline__ float block_sum(float v, float* sh) {
 // validates the previous column, sums its 17 embedding rows in fp32 in row order
 // (text row first), and tabulates cos/sin of this frame's RoPE angles from fp64.
 __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x;
   __shared__ int col[kRows];
   __shared__ int live_s, pos_s;
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
 }
 
 cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s) {
-  k_begin<<<D.B, 256, 0, s>>>(D, b);
+  { cudaError_t e_ = launch_k(k_begin, dim3(D.B), dim3(256), 0, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const float* __restrict__ x, in
                                                  const float* __restrict__ alpha, int K,
                                                  float eps, float* __restrict__ out, int ldo,
                                                  uint16_t* __restrict__ op, int Bp) {
+  pdl_wait_and_trigger();
   __shared__ float sh[17];
   const int b = blockIdx.x;
   const float* xr = x + (size_t)b * ldx;
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const float* __restrict__ x, in
 
 cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
                            float* out, int ldo, uint16_t* op, cudaStream_t s) {
-  k_rmsnorm<<<D.B, 512, 0, s>>>(x, ldx, alpha, K, D.eps, out, ldo, op, D.Bp);
+  { cudaError_t e_ = launch_k(k_rmsnorm, dim3(D.B), dim3(512), 0, s, 1, x, ldx, alpha, K, D.eps, out, ldo, op, D.Bp); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -144,6 +146,7 @@ cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* 
 // by log2(e)/sqrt(Dh) (the attention kernel works in base 2); k is rotated; k and v are
 // rounded to bf16 into ring index pos mod W of this layer's ring.
 __global__ void k_rope_ring(Dims D, Buffers b, int layer) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
   if (!b.live[s] || i >= D.Dh / 2) return;
   const int p = b.pos[s];
@@ -168,7 +171,7 @@ __global__ void k_rope_ring(Dims D, Buffers b, int layer) {
 }
 
 cudaError_t launch_rope_ring(const Dims& D, const Buffers& b, int layer, cudaStream_t s) {
-  k_rope_ring<<<dim3(D.B, D.H), (D.Dh / 2 + 31) / 32 * 32, 0, s>>>(D, b, layer);
+  { cudaError_t e_ = launch_k(k_rope_ring, dim3(dim3(D.B, D.H)), dim3((D.Dh / 2 + 31) / 32 * 32), 0, s, 1, D, b, layer); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -217,6 +220,7 @@ __device__ int block_argmax(const float* __restrict__ lg, int n, uint32_t* statu
 }
 
 __global__ void __launch_bounds__(1024) k_text_argmax(Dims D, Buffers b) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x;
   if (!b.live[s]) {
     if (threadIdx.x == 0) { b.out_col[s * kRows] = -1; b.tok[s] = 0; }
@@ -235,13 +239,14 @@ __global__ void __launch_bounds__(1024) k_text_argmax(Dims D, Buffers b) {
 }
 
 cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s) {
-  k_text_argmax<<<D.B, 1024, 0, s>>>(D, b);
+  { cudaError_t e_ = launch_k(k_text_argmax, dim3(D.B), dim3(1024), 0, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 // Step k of the depformer decides row k+1: agent rows 1..8 are greedy unless forced,
 // user rows 9..16 take this frame's user codes.
 __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x, row = step + 1;
   if (!b.live[s]) {
     if (threadIdx.x == 0) { b.out_col[s * kRows + row] = -1; b.tok[s] = 0; }
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step
 }
 
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s) {
-  k_dep_argmax<<<D.B, 1024, 0, s>>>(D, b, step);
+  { cudaError_t e_ = launch_k(k_dep_argmax, dim3(D.B), dim3(1024), 0, s, 1, D, b, step); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
@@ -274,6 +279,7 @@ cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStr
 // indexed by step, so a new frame overwrites it from step 0 (reset each frame).
 template <int E>  // head dim / 32
 __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
   float* out = b.dout + (size_t)s * D.dd + h * D.Dhd;
@@ -295,6 +301,17 @@ __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
     cache[(size_t)step * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kk[e];
     cache[(size_t)step * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] = vv[e];
   }
+  // preload this frame's earlier steps (independent loads), then attend in step order
+  float kc[16][E], vc[16][E];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    if (t >= step) break;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      kc[t][e] = cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
+      vc[t][e] = cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
+    }
+  }
   const float scale = 1.0f / sqrtf((float)D.Dhd);
   float sc[16];
   float m = -INFINITY;
@@ -303,10 +320,7 @@ __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
     if (t > step) break;
     float dot = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float kv = (t == step) ? kk[e] : cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
-      dot = fmaf(q[e], kv, dot);
-    }
+    for (int e = 0; e < E; ++e) dot = fmaf(q[e], (t == step) ? kk[e] : kc[t][e], dot);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
     sc[t] = dot * scale;
@@ -321,10 +335,7 @@ __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
     const float p = expf(sc[t] - m);
     l += p;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float vx = (t == step) ? vv[e] : cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
-      acc[e] = fmaf(p, vx, acc[e]);
-    }
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(p, (t == step) ? vv[e] : vc[t][e], acc[e]);
   }
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -338,9 +349,9 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
                             cudaStream_t s) {
   const int threads = D.Hd * 32;
   switch (D.Dhd) {
-    case 32: k_dep_attn<1><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
-    case 64: k_dep_attn<2><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
-    case 128: k_dep_attn<4><<<D.B, threads, 0, s>>>(D, b, step, layer, op); break;
+    case 32: { cudaError_t e_ = launch_k(k_dep_attn<1>, dim3(D.B), dim3(threads), 0, s, 1, D, b, step, layer, op); if (e_ != cudaSuccess) return e_; } break;
+    case 64: { cudaError_t e_ = launch_k(k_dep_attn<2>, dim3(D.B), dim3(threads), 0, s, 1, D, b, step, layer, op); if (e_ != cudaSuccess) return e_; } break;
+    case 128: { cudaError_t e_ = launch_k(k_dep_attn<4>, dim3(D.B), dim3(threads), 0, s, 1, D, b, step, layer, op); if (e_ != cudaSuccess) return e_; } break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -348,6 +359,7 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
 
 // ---- end of tick -----------------------------------------------------------------------
 __global__ void k_finish(Dims D, Buffers b) {
+  pdl_wait_and_trigger();
   const int s = blockIdx.x, r = threadIdx.x;
   if (!b.live[s]) {
     if (r < kRows) b.out_col[s * kRows + r] = -1;
@@ -357,7 +369,7 @@ __global__ void k_finish(Dims D, Buffers b) {
 }
 
 cudaError_t launch_finish(const Dims& D, const Buffers& b, cudaStream_t s) {
-  k_finish<<<D.B, 32, 0, s>>>(D, b);
+  { cudaError_t e_ = launch_k(k_finish, dim3(D.B), dim3(32), 0, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -10,19 +10,22 @@
 // weight byte once, so the extra N columns cost tensor-core time only, which a
 // weight-streaming kernel has to spare.
 //
-// One CTA = one (M-tile, K-split) unit, 4 warps, two CTAs per SM:
+// One CTA = one (M-tile, K-split) unit, 4 warps, two CTAs per SM; the splits of a tile
+// are one cluster:
 //   warp 0 lane 0  TMA producer: weight tile (two 64-row boxes) + activation tile per
 //                  64-wide k-block into a ring of shared-memory stages (128B swizzle);
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per k-block into a TMEM
 //                  accumulator [128 lanes x N columns], tcgen05.commit frees the stage;
 //   all 4 warps    epilogue: tcgen05.ld of their 32 TMEM lanes, hi + lo, then either
-//                  the final epilogue (one split) or an fp32 partial; the last CTA of
-//                  an M-tile (atomic ticket) adds the partials in split order and runs
-//                  the final epilogue.  The split count depends only on the matrix
-//                  shape and the SM count, never on the batch, so a session's bits do
-//                  not depend on the other sessions.
+//                  the final epilogue (one split) or, when the K range is split, a
+//                  reduction across the thread-block cluster formed by the tile's
+//                  splits: partials meet in distributed shared memory and each CTA
+//                  adds them in split order for a slice of the tile's rows.  The split
+//                  count depends only on the matrix shape and the SM count, never on
+//                  the batch, so a session's bits do not depend on the other sessions.
 // Every mbarrier wait is bounded; on expiry the kernel raises PP_S_TIMEOUT, drains
 // its own copies (bounded), frees its TMEM and returns.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <math.h>
 
@@ -102,18 +105,38 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
-  uint32_t r[8];
+// 8 consecutive accumulator columns of this thread's TMEM lane (no wait).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t r[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Orders a register after the preceding tcgen05.wait::ld (volatile asms keep their order).
+__device__ __forceinline__ float after_wait(uint32_t r) {
+  asm volatile("" : "+r"(r));
+  return __uint_as_float(r);
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+namespace cg = cooperative_groups;
+
+__device__ __forceinline__ void epi_store(const UmmaArgs& a, int b, int m, float v) {
+  float* y = a.Y + (size_t)b * a.ldy + m;
+  if (a.epi == EPI_STORE) {
+    *y = v;
+  } else if (a.epi == EPI_ADD) {
+    *y = v + *y;
+  } else {  // EPI_EMB
+    *y = v + bf16_to_f32(a.emb[(size_t)a.tok[b] * a.M + m]);
+  }
+}
 
 template <int N>
 struct Cfg {
@@ -137,8 +160,8 @@ __global__ void __launch_bounds__(128, 2)
   // bars[0..S) full, bars[S..2S) empty, bars[2S] done; then the TMEM address and flags
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
+  pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
   const int kb0 = (int)(((long long)sp * a.kblocks) / a.splits);
@@ -237,91 +260,113 @@ __global__ void __launch_bounds__(128, 2)
   const bool row_ok = a.pair_rows ? (m < a.pair_rows) : (m < a.M);
 
   float acc[N / 2];
-#pragma unroll
-  for (int c = 0; c < N / 2; c += 8) {
-    float hi[8], lo[8];
+  {
+    uint32_t hi[N / 2], lo[N / 2];
     const uint32_t t = tmem + ((uint32_t)(warp * 32) << 16);
     if (ok) {
-      tmem_ld8(t + c, hi);
-      tmem_ld8(t + Bp + c, lo);
+#pragma unroll
+      for (int c = 0; c < N / 2; c += 8) {
+        tmem_ld8(t + c, hi + c);
+        tmem_ld8(t + Bp + c, lo + c);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < N / 2; ++c) acc[c] = after_wait(hi[c]) + after_wait(lo[c]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) hi[j] = lo[j] = 0.f;
+      for (int c = 0; c < N / 2; ++c) acc[c] = 0.f;
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[c + j] = hi[j] + lo[j];
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols));
-  if (!ok) {
-    if (threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
-    return;
-  }
+  if (!ok && a.splits == 1 && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
 
-  // split-K: partial [split][b][tile row] then the last CTA of the tile reduces in order
-  if (a.splits > 1) {
-    float* part = a.partial + (size_t)mt * a.splits * B * 128;
+  // ---- final epilogue, single split: straight from the accumulator registers ------------
+  if (a.splits == 1) {
+    if (!ok) return;
+    if (a.epi == EPI_SILU) {
+      float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
+      if (r >= 64) {
 #pragma unroll
-    for (int b = 0; b < N / 2; ++b)
-      if (b < B) part[((size_t)sp * B + b) * 128 + r] = acc[b];
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const unsigned prev = atomicAdd(a.counter + mt, 1u);
-      *last_flag = (prev == (unsigned)(a.splits - 1));
-    }
-    __syncthreads();
-    if (!*last_flag) return;
-    __threadfence();
+        for (int b = 0; b < N / 2; ++b)
+          if (b < B) xch[(r - 64) * Bp + b] = acc[b];
+      }
+      __syncthreads();
+      if (r < 64 && row_ok) {
 #pragma unroll
-    for (int b = 0; b < N / 2; ++b) acc[b] = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-#pragma unroll
-      for (int b = 0; b < N / 2; ++b)
-        if (b < B) acc[b] += __ldcg(part + ((size_t)s * B + b) * 128 + r);
-    }
-    if (threadIdx.x == 0) a.counter[mt] = 0u;
-  }
-
-  // ---- final epilogue ------------------------------------------------------------------
-  if (a.epi == EPI_SILU) {
-    float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
-    if (r >= 64) {
-#pragma unroll
-      for (int b = 0; b < N / 2; ++b)
-        if (b < B) xch[(r - 64) * Bp + b] = acc[b];
-    }
-    __syncthreads();
-    if (r < 64 && row_ok) {
-#pragma unroll
-      for (int b = 0; b < N / 2; ++b) {
-        if (b < B) {
-          const float g = acc[b], u = xch[r * Bp + b];
-          op_store(a.op_out, a.ld_op, a.Bp_out, b, m, g / (1.0f + expf(-g)) * u);
+        for (int b = 0; b < N / 2; ++b) {
+          if (b < B) {
+            const float g = acc[b], u = xch[r * Bp + b];
+            op_store(a.op_out, a.ld_op, a.Bp_out, b, m, g / (1.0f + expf(-g)) * u);
+          }
         }
       }
+      return;
     }
+    if (!row_ok) return;
+#pragma unroll
+    for (int b = 0; b < N / 2; ++b)
+      if (b < B) epi_store(a, b, m, acc[b]);
     return;
   }
-  if (!row_ok) return;
+
+  // ---- split-K across the thread-block cluster (one CTA per split of this tile) ----------
+  // Each CTA parks its partial [128 rows][B] in its own shared memory; after a cluster
+  // barrier, CTA `sp` reduces a slice of the tile's rows by reading the S partials
+  // through distributed shared memory in split order 0..S-1, and applies the epilogue.
+  // Every CTA passes both cluster barriers, also after a timeout.
+  constexpr int PB = N / 2 + 1;                     // padded row stride of a partial
+  float* mine = reinterpret_cast<float*>(smem);
 #pragma unroll
-  for (int b = 0; b < N / 2; ++b) {
-    if (b >= B) continue;
-    float v = acc[b];
-    float* y = a.Y + (size_t)b * a.ldy + m;
-    if (a.epi == EPI_STORE) {
-      *y = v;
-    } else if (a.epi == EPI_ADD) {
-      v += *y;
-      *y = v;
-    } else {  // EPI_EMB
-      v += bf16_to_f32(a.emb[(size_t)a.tok[b] * a.M + m]);
-      *y = v;
+  for (int b = 0; b < N / 2; ++b)
+    if (b < B) mine[r * PB + b] = ok ? acc[b] : 0.f;
+  cg::cluster_group cluster = cg::this_cluster();
+  cluster.sync();
+  const int S = a.splits;
+  const float* peer[kMaxSplits];
+#pragma unroll
+  for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? cluster.map_shared_rank(mine, q) : mine;
+  if (a.epi == EPI_SILU) {
+    const int p0 = (sp * 64) / S, p1 = ((sp + 1) * 64) / S;
+    const int n = (p1 - p0) * B;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int p = p0 + e / B, b = e % B;
+      float gv[kMaxSplits], uv[kMaxSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxSplits; ++q)
+        if (q < S) {
+          gv[q] = peer[q][p * PB + b];
+          uv[q] = peer[q][(p + 64) * PB + b];
+        }
+      float g = 0.f, u = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxSplits; ++q)
+        if (q < S) { g += gv[q]; u += uv[q]; }
+      const int mm = mt * 64 + p;
+      if (mm < a.pair_rows) op_store(a.op_out, a.ld_op, a.Bp_out, b, mm, g / (1.0f + expf(-g)) * u);
+    }
+  } else {
+    const int r0 = (sp * 128) / S, r1 = ((sp + 1) * 128) / S;
+    const int n = (r1 - r0) * B;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int rr = r0 + e / B, b = e % B;
+      float pv[kMaxSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxSplits; ++q)
+        if (q < S) pv[q] = peer[q][rr * PB + b];
+      float v = 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxSplits; ++q)
+        if (q < S) v += pv[q];
+      const int mm = mt * 128 + rr;
+      if (mm < a.M) epi_store(a, b, mm, v);
     }
   }
+  cluster.sync();   // peers may still be reading this CTA's partial until here
+  if (!ok && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
 }
 
 }  // namespace
@@ -330,8 +375,7 @@ template <int N>
 static cudaError_t umma_n(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                           cudaStream_t s) {
   const int grid = a.m_tiles * a.splits;
-  k_umma<N><<<grid, 128, Cfg<N>::kSmem, s>>>(a, mA, mB);
-  return cudaGetLastError();
+  return launch_k(k_umma<N>, dim3(grid), dim3(128), Cfg<N>::kSmem, s, a.splits, a, mA, mB);
 }
 
 template <int N>

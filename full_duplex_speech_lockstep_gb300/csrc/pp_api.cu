@@ -9,6 +9,10 @@
 
 using namespace pp;
 
+namespace pp {
+bool g_use_pdl = false;
+}
+
 // Timing events recorded at every kernel boundary of the profiling graph.
 struct Prof {
   std::vector<cudaEvent_t> ev;
@@ -43,6 +47,7 @@ struct pp_engine {
   Dims D;
   Buffers buf;
   bool tensor = true;
+  bool pdl = true;
   Mm mm[MM_COUNT];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
@@ -144,8 +149,6 @@ size_t carve(const Dims& D, char* base, Buffers* b) {
   b->op_dd = cv.take<uint16_t>(R * D.dd);
   b->op_do = cv.take<uint16_t>(R * D.dd);
   b->op_fd = cv.take<uint16_t>(R * D.Fd);
-  b->tile_count = cv.take<uint32_t>(kMaxTiles);
-  b->partial = cv.take<float>((size_t)kMaxUnits * 128 * B);
   return (cv.off + 255) & ~(size_t)255;
 }
 
@@ -193,7 +196,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k, uint3
 int choose_splits(int m_tiles, int kblocks, int slots) {
   int best = 1;
   double best_t = 1e300;
-  for (int sp = 1; sp <= kblocks && m_tiles * sp <= kMaxUnits; ++sp) {
+  for (int sp = 1; sp <= kblocks && sp <= kMaxSplits && m_tiles * sp <= kMaxUnits; ++sp) {
     const int units = m_tiles * sp;
     const int waves = (units + slots - 1) / slots;
     const double t = waves * ((double)((kblocks + sp - 1) / sp) + 3.0);
@@ -254,8 +257,6 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   a.op_out = op_out;
   a.ld_op = ld_op;
   a.Bp_out = D.Bp;
-  a.partial = b.partial;
-  a.counter = b.tile_count;
   a.status = b.status;
   return launch_umma(a, g.mapA, g.mapB, s);
 }
@@ -299,34 +300,34 @@ cudaError_t enqueue_tick_tensor(const pp_engine* e, cudaStream_t s, Prof* prof) 
   for (int k = 0; k < D.nq; ++k) {
     const uint16_t* emb =
         (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_INPROJ);
     PP_TRY(mm_launch(D, b, mm[MM_DIN], k * D.dd, EPI_EMB, b.y, D.dd, emb, nullptr, 0, s));
     for (int j = 0; j < D.Ld; ++j) {
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_NORM);
       PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
                             b.op_dd, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_QKV);
       PP_TRY(mm_launch(D, b, mm[MM_DQKV], j * 3 * D.dd, EPI_STORE, b.dqkv, 3 * D.dd, nullptr,
                        nullptr, 0, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_ATTN);
       PP_TRY(launch_dep_attn(D, b, k, j, true, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_OPROJ);
       PP_TRY(mm_launch(D, b, mm[MM_DO], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_NORM);
       PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
                             b.op_dd, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_GATEUP);
       PP_TRY(mm_launch(D, b, mm[MM_DGU], j * 2 * D.Fd, EPI_SILU, nullptr, 0, nullptr, b.op_fd,
                        D.Fd, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_DOWN);
       PP_TRY(mm_launch(D, b, mm[MM_DDOWN], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
     }
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_NORM);
     PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, nullptr, 0, b.op_dd, s));
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_HEAD);
     PP_TRY(mm_launch(D, b, mm[MM_DHEAD], k * D.Va, EPI_STORE, b.logits + D.Vt + (size_t)k * D.Va,
                      D.logits_ld, nullptr, nullptr, 0, s));
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
   }
   MARK(PP_K_FINISH);
@@ -387,45 +388,45 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
     a.X = b.z; a.ldx = D.d; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_EMB;
     a.emb = (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
     a.tok = b.tok;
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_INPROJ);
     PP_TRY(launch_gemv(D, a, s));
     for (int j = 0; j < D.Ld; ++j) {
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_NORM);
     PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, nullptr, s));
       a = GemvArgs{};
       a.W = b.dep_wqkv + (size_t)j * 3 * D.dd * D.dd; a.M = 3 * D.dd; a.K = D.dd;
       a.X = b.yn; a.ldx = D.dd; a.Y = b.dqkv; a.ldy = 3 * D.dd; a.epi = EPI_STORE;
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_QKV);
     PP_TRY(launch_gemv(D, a, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_ATTN);
     PP_TRY(launch_dep_attn(D, b, k, j, false, s));
       a = GemvArgs{};
       a.W = b.dep_wo + (size_t)j * D.dd * D.dd; a.M = D.dd; a.K = D.dd;
       a.X = b.dout; a.ldx = D.dd; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_ADD;
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_OPROJ);
     PP_TRY(launch_gemv(D, a, s));
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_NORM);
     PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, b.yn, D.dd, nullptr, s));
       a = GemvArgs{};
       a.W = b.dep_wgu + (size_t)j * 2 * D.Fd * D.dd; a.M = D.Fd; a.K = D.dd;
       a.X = b.yn; a.ldx = D.dd; a.Y = b.dh; a.ldy = D.Fd; a.epi = EPI_SILU;
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_GATEUP);
     PP_TRY(launch_gemv(D, a, s));
       a = GemvArgs{};
       a.W = b.dep_wdown + (size_t)j * D.dd * D.Fd; a.M = D.dd; a.K = D.Fd;
       a.X = b.dh; a.ldx = D.Fd; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_ADD;
-      MARK(PP_K_DEPFORMER);
+      MARK(PP_K_DEP_DOWN);
     PP_TRY(launch_gemv(D, a, s));
     }
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_NORM);
     PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, b.yn, D.dd, nullptr, s));
     a = GemvArgs{};
     a.W = b.dep_heads + (size_t)k * D.Va * D.dd; a.M = D.Va; a.K = D.dd;
     a.X = b.yn; a.ldx = D.dd; a.Y = b.logits + D.Vt + (size_t)k * D.Va; a.ldy = D.logits_ld;
     a.epi = EPI_STORE;
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_gemv(D, a, s));
-    MARK(PP_K_DEPFORMER);
+    MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
   }
   MARK(PP_K_FINISH);
@@ -533,14 +534,15 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   e->open.assign(D.B, 0);
 
   e->tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
+  g_use_pdl = (c->flags & PP_FLAG_PDL) != 0;   // read while this engine's graphs are captured
   cudaError_t err = cudaSuccess;
   // zero the small state (positions, liveness, control, status, attention counters)
   char* small_lo = reinterpret_cast<char*>(b.pos);
   char* small_hi = reinterpret_cast<char*>(b.in_col);
   err = cudaMemset(small_lo, 0, (size_t)(small_hi - small_lo));
-  if (err == cudaSuccess) {   // operands (their padding rows stay zero) and split-K tickets
+  if (err == cudaSuccess) {   // operands: their padding rows stay zero
     char* op_lo = reinterpret_cast<char*>(b.op_d);
-    char* op_hi = reinterpret_cast<char*>(b.partial);
+    char* op_hi = reinterpret_cast<char*>(b.op_fd + 2 * (size_t)D.Bp * D.Fd);
     err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
   }
   if (err == cudaSuccess && e->tensor) {
@@ -552,6 +554,7 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
     if (err == cudaSuccess && !plan_all(e, 2 * nsm)) err = cudaErrorInvalidValue;
   }
   if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking);
+  e->pdl = g_use_pdl;
   if (err == cudaSuccess)
     err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
   if (err == cudaSuccess) {
@@ -692,6 +695,7 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
                     float* logits, void* stream, double* kind_ms, int64_t* kind_launches) {
   if (!e || !kind_ms || !kind_launches) return PP_EINVAL;
   if (!e->prof_exec) {   // capture the profiling graph on first use
+    g_use_pdl = e->pdl;
     cudaError_t err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
     if (err == cudaSuccess) {
       cudaError_t le = enqueue_tick(e, e->cap_stream, &e->prof);

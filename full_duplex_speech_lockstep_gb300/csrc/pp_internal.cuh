@@ -85,12 +85,50 @@ struct Buffers {
   uint16_t* op_dd;         // K = dd  (normalised depformer stream)
   uint16_t* op_do;         // K = dd  (depformer attention output)
   uint16_t* op_fd;         // K = Fd  (depformer gated hidden)
-  float* partial;          // split-K partials of the tensor-core contractions
-  uint32_t* tile_count;    // split-K tickets per M-tile
 };
 
-constexpr int kMaxUnits = 2048;      // cap on (M-tile x K-split) units of one contraction
-constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction (ticket array)
+constexpr int kMaxUnits = 4096;      // cap on (M-tile x K-split) units of one contraction
+constexpr int kMaxSplits = 8;        // K-splits of one tile form one (portable) cluster
+constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction
+
+// ---- programmatic dependent launch ------------------------------------------------------
+// Every kernel of the tick is launched with programmatic stream serialization: it may
+// start while its predecessor drains, waits (griddepcontrol.wait) for the predecessor's
+// completion and memory flush before touching any data, and lets its own successor
+// launch right away.
+__device__ __forceinline__ void pdl_wait_and_trigger() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+extern bool g_use_pdl;   // set by the engine before it captures a tick
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (g_use_pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = (unsigned)cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // ---- launchers (stream-ordered; return cudaGetLastError) ----------------------------
 cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s);
@@ -127,8 +165,6 @@ struct UmmaArgs {
   uint16_t* op_out;    // EPI_SILU: operand [2*Bp_out][ld_op] of the next contraction
   int ld_op;
   int Bp_out;
-  float* partial;
-  uint32_t* counter;
   uint32_t* status;
 };
 cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,

@@ -78,6 +78,10 @@ typedef struct {
  * tcgen05 tensor-core path (split-bf16 activations).  The two paths round
  * differently, so a session's bits are reproducible within one path only. */
 #define PP_FLAG_CUDA_CORE_GEMM 0x1
+/* Launch the tick's kernels with programmatic dependent launch (each kernel may start
+ * while its predecessor drains and waits for it in-kernel).  Off by default: on GB300
+ * the tick measured faster without it. */
+#define PP_FLAG_PDL 0x2
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */
@@ -193,7 +197,14 @@ enum pp_kernel_kind {
   PP_K_GATEUP,      /* gate/up projection + SiLU gating */
   PP_K_DOWN,        /* down-projection + residual */
   PP_K_TEXT_HEAD,   /* final norm, text head, greedy text token */
-  PP_K_DEPFORMER,   /* every kernel of the 16 depformer steps */
+  PP_K_DEP_INPROJ,  /* depformer: per-codebook input projection + token embedding */
+  PP_K_DEP_NORM,    /* depformer: RMSNorms */
+  PP_K_DEP_QKV,     /* depformer: QKV projection */
+  PP_K_DEP_ATTN,    /* depformer: attention over the frame's steps */
+  PP_K_DEP_OPROJ,   /* depformer: out-projection + residual */
+  PP_K_DEP_GATEUP,  /* depformer: gate/up projection + SiLU gating */
+  PP_K_DEP_DOWN,    /* depformer: down-projection + residual */
+  PP_K_DEP_HEAD,    /* depformer: per-codebook head + greedy / forced / user row */
   PP_K_FINISH,      /* end-of-tick bookkeeping */
   PP_K_COUNT
 };
