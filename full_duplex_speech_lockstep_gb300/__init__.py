@@ -35,7 +35,7 @@ PP_W_COUNT = len(WEIGHT_NAMES)
 EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_session_open", "pp_session_close", "pp_session_import", "pp_session_pos",
            "pp_ring_block", "pp_step", "pp_step_host", "pp_status", "pp_step_kernel_count",
-           "pp_profile_step"]
+           "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -57,6 +57,7 @@ class pp_config(ctypes.Structure):
 
 PP_FLAG_CUDA_CORE_GEMM = 0x1
 PP_FLAG_PDL = 0x2
+PP_FLAG_TWO_GROUPS = 0x4
 
 
 class pp_weights(ctypes.Structure):
@@ -103,6 +104,10 @@ def lib():
         L.pp_step_kernel_count.restype = I
         L.pp_profile_step.argtypes = [P] * 10
         L.pp_profile_step.restype = I
+        L.pp_ring_attention_scratch_bytes.argtypes = [I, I, I, I]
+        L.pp_ring_attention_scratch_bytes.restype = ctypes.c_size_t
+        L.pp_ring_attention.argtypes = [P, P, P, I64, P, I, I, I, I, P, P, ctypes.c_size_t, P]
+        L.pp_ring_attention.restype = I
         _lib = L
     return _lib
 
@@ -202,6 +207,20 @@ def pp_profile_step(h, prev_column, user_codes, force_mask, forced_tokens, colum
     return _check("pp_profile_step", lib().pp_profile_step(
         h, prev_column, user_codes, force_mask, forced_tokens, column, logits, stream,
         kind_ms, kind_launches))
+
+
+def pp_ring_attention_scratch_bytes(B, H, head_dim, window):
+    n = lib().pp_ring_attention_scratch_bytes(B, H, head_dim, window)
+    if n == 0:
+        raise PPError("pp_ring_attention_scratch_bytes", PP_EINVAL)
+    return n
+
+
+def pp_ring_attention(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, scratch,
+                      scratch_bytes, stream):
+    return _check("pp_ring_attention", lib().pp_ring_attention(
+        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, scratch, scratch_bytes,
+        stream))
 
 
 # ---- convenience wrapper over torch device memory ---------------------------------------

@@ -38,7 +38,7 @@ __device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
 }
 
 template <int DH>
-__global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int layer, bool op) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 4) k_attn(AttnArgs a) {
   pdl_wait_and_trigger();
   constexpr int PIECES = DH / 8;        // 16-byte pieces per K/V row
   constexpr int LOADS = PIECES / 4;     // pieces per lane (4 lanes per key)
@@ -47,26 +47,27 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
   const int c = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, qd = lane & 3;
-  float* o_out = b.o + (size_t)s * D.d + h * DH;
+  const int HD = a.H * DH;
+  float* o_out = a.out + (size_t)s * a.out_ld + h * DH;
 
-  if (!b.live[s]) {
+  const int n = min(a.n_valid[s], a.W);   // never read past the W ring positions
+  if (n <= 0) {   // closed slot: zero output
     if (c == 0)
       for (int i = threadIdx.x; i < DH; i += blockDim.x) {
         o_out[i] = 0.f;
-        if (op) op_store(b.op_o, D.d, D.Bp, s, h * DH + i, 0.f);
+        if (a.op) op_store(a.op, HD, a.op_Bp, s, h * DH + i, 0.f);
       }
     return;
   }
-  const int n = min(b.pos[s] + 1, D.W);
   const int nc = (n + kAttnChunk - 1) / kAttnChunk;
   if (c >= nc) return;
 
-  const size_t blk = (size_t)D.W * DH;
-  const uint16_t* Kh = b.ring + ((((size_t)layer * D.B + s) * 2 + 0) * D.H + h) * blk;
-  const uint16_t* Vh = b.ring + ((((size_t)layer * D.B + s) * 2 + 1) * D.H + h) * blk;
+  const size_t blk = (size_t)a.W * DH;
+  const uint16_t* Kh = a.k + (size_t)s * a.slot_stride + h * blk;
+  const uint16_t* Vh = a.v + (size_t)s * a.slot_stride + h * blk;
 
   float q[LOADS][8];
-  const float* qp = b.q + (size_t)s * D.d + h * DH;
+  const float* qp = a.q + (size_t)s * a.q_ld + h * DH;
 #pragma unroll
   for (int j = 0; j < LOADS; ++j) {
     const float4* p4 = reinterpret_cast<const float4*>(qp + (j * 4 + qd) * 8);
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
     }
     dot += __shfl_xor_sync(0xffffffffu, dot, 1);
     dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-    sc[it] = (key0 + it * 8 + g < n) ? dot : -INFINITY;
+    sc[it] = (key0 + it * 8 + g < n) ? dot * a.q_scale : -INFINITY;
   }
   float m = sc[0];
 #pragma unroll
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
   __syncthreads();
 
   // chunk partial: merge the warps in warp order
-  float* part = b.attn_part + (((size_t)s * D.H + h) * D.nc_max) * (DH + 2);
+  float* part = a.part + (((size_t)s * a.H + h) * a.nc_max) * (DH + 2);
   {
     float M = sm_m[0];
     for (int w = 1; w < kAttnWarps; ++w) M = fmaxf(M, sm_m[w]);
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(b.attn_count + (size_t)s * D.H + h, 1u);
+    const unsigned prev = atomicAdd(a.count + (size_t)s * a.H + h, 1u);
     sm_last = (prev == (unsigned)(nc - 1));
   }
   __syncthreads();
@@ -198,22 +199,44 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn(Dims D, Buffers b, int
       O = fmaf(f, __ldcg(src + 2 + i), O);
     }
     o_out[i] = O / L;
-    if (op) op_store(b.op_o, D.d, D.Bp, s, h * DH + i, O / L);
+    if (a.op) op_store(a.op, HD, a.op_Bp, s, h * DH + i, O / L);
   }
-  if (threadIdx.x == 0) b.attn_count[(size_t)s * D.H + h] = 0u;
+  if (threadIdx.x == 0) a.count[(size_t)s * a.H + h] = 0u;
 }
 
 }  // namespace
 
-cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s) {
-  const dim3 grid(D.nc_max, D.H, D.B);
-  switch (D.Dh) {
-    case 32: { cudaError_t e_ = launch_k(k_attn<32>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
-    case 64: { cudaError_t e_ = launch_k(k_attn<64>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
-    case 128: { cudaError_t e_ = launch_k(k_attn<128>, dim3(grid), dim3(kAttnWarps * 32), 0, s, 1, D, b, layer, op); if (e_ != cudaSuccess) return e_; } break;
+cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, cudaStream_t s) {
+  const dim3 grid(a.nc_max, a.H, B);
+  switch (Dh) {
+    case 32: return launch_k(k_attn<32>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
+    case 64: return launch_k(k_attn<64>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
+    case 128: return launch_k(k_attn<128>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+}
+
+// The tick's attention for one layer: the slot's rotated, pre-scaled q against its ring.
+cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s) {
+  AttnArgs a{};
+  a.q = b.q;
+  a.q_ld = D.d;
+  a.q_scale = 1.0f;   // q already carries log2(e) / sqrt(Dh)
+  const size_t blk = (size_t)D.W * D.Dh;
+  a.k = b.ring + ((size_t)layer * D.B * 2 + 0) * D.H * blk;
+  a.v = a.k + (size_t)D.H * blk;
+  a.slot_stride = 2 * (size_t)D.H * blk;
+  a.n_valid = b.nvalid;
+  a.H = D.H;
+  a.W = D.W;
+  a.nc_max = D.nc_max;
+  a.out = b.o;
+  a.out_ld = D.d;
+  a.op = op ? b.op_o : nullptr;
+  a.op_Bp = D.Bp;
+  a.part = b.attn_part;
+  a.count = b.attn_count;
+  return launch_attn_args(a, D.B, D.Dh, s);
 }
 
 }  // namespace pp

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
     b.live[s] = c & 1;
     live_s = c & 1;
     pos_s = b.pos[s];
+    b.nvalid[s] = live_s ? min(pos_s + 1, D.W) : 0;
   }
   __syncthreads();
   if (threadIdx.x < kRows) {

@@ -127,6 +127,13 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_floa
 
 namespace cg = cooperative_groups;
 
+// The value the epilogue adds to the contraction: 0 (EPI_STORE), the residual (EPI_ADD)
+// or the token embedding row (EPI_EMB).
+__device__ __forceinline__ float epi_extra(const UmmaArgs& a, int b, int m) {
+  if (a.epi == EPI_ADD) return a.Y[(size_t)b * a.ldy + m];
+  return bf16_to_f32(a.emb[(size_t)a.tok[b] * a.M + m]);
+}
+
 __device__ __forceinline__ void epi_store(const UmmaArgs& a, int b, int m, float v) {
   float* y = a.Y + (size_t)b * a.ldy + m;
   if (a.epi == EPI_STORE) {
@@ -349,20 +356,41 @@ __global__ void __launch_bounds__(128, 2)
       if (mm < a.pair_rows) op_store(a.op_out, a.ld_op, a.Bp_out, b, mm, g / (1.0f + expf(-g)) * u);
     }
   } else {
+    // this CTA's slice of rows, processed 8 elements per pass so that up to 8*S
+    // distributed-shared-memory loads (and the residual loads) are in flight at once
     const int r0 = (sp * 128) / S, r1 = ((sp + 1) * 128) / S;
     const int n = (r1 - r0) * B;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const int rr = r0 + e / B, b = e % B;
-      float pv[kMaxSplits];
+    constexpr int CH = 8;
+    for (int e0 = threadIdx.x; e0 < n; e0 += CH * (int)blockDim.x) {
+      int off[CH], mrow[CH], bcol[CH];
 #pragma unroll
-      for (int q = 0; q < kMaxSplits; ++q)
-        if (q < S) pv[q] = peer[q][rr * PB + b];
-      float v = 0.f;
+      for (int i = 0; i < CH; ++i) {
+        const int e = e0 + i * (int)blockDim.x;
+        const int rr = r0 + e / B;
+        bcol[i] = e % B;
+        mrow[i] = (e < n) ? mt * 128 + rr : a.M;     // a.M marks "no element"
+        off[i] = rr * PB + bcol[i];
+      }
+      float ex[CH];
 #pragma unroll
-      for (int q = 0; q < kMaxSplits; ++q)
-        if (q < S) v += pv[q];
-      const int mm = mt * 128 + rr;
-      if (mm < a.M) epi_store(a, b, mm, v);
+      for (int i = 0; i < CH; ++i)
+        ex[i] = (a.epi != EPI_STORE && mrow[i] < a.M) ? epi_extra(a, bcol[i], mrow[i]) : 0.f;
+      float pv[CH][kMaxSplits];
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q)
+          if (q < S && mrow[i] < a.M) pv[i][q] = peer[q][off[i]];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        if (mrow[i] < a.M) {
+          float v = 0.f;
+#pragma unroll
+          for (int q = 0; q < kMaxSplits; ++q)
+            if (q < S) v += pv[i][q];
+          a.Y[(size_t)bcol[i] * a.ldy + mrow[i]] = v + ex[i];
+        }
+      }
     }
   }
   cluster.sync();   // peers may still be reading this CTA's partial until here

@@ -1,5 +1,6 @@
 // pp_api.cu - the C ABI (include/pp.h): engine creation over caller-owned weights and
 // workspace, the session table, and one lockstep tick captured as a CUDA graph.
+#include <math.h>
 #include <string.h>
 
 #include <new>
@@ -11,6 +12,7 @@ using namespace pp;
 
 namespace pp {
 bool g_use_pdl = false;
+int g_launch_priority = 0;
 }
 
 // Timing events recorded at every kernel boundary of the profiling graph.
@@ -42,13 +44,32 @@ struct Mm {
 enum MmKind { MM_QKV, MM_O, MM_GU, MM_DOWN, MM_TEXT, MM_DIN, MM_DQKV, MM_DO, MM_DGU, MM_DDOWN,
               MM_DHEAD, MM_COUNT };
 
-struct pp_engine {
-  pp_config cfg;
+constexpr int kMaxGroups = 2;
+
+// A group is a contiguous range of slots run as one independent chain of kernels (its
+// own ring, activations, operands and contraction plans).  With two groups the tick
+// graph has two parallel branches: one group's latency-bound depformer overlaps the
+// other group's bandwidth-bound attention.  Every kernel computes each slot the same
+// way whatever the group size, so grouping does not change any session's bits.
+struct Group {
+  int slot0 = 0;
   Dims D;
   Buffers buf;
+  Mm mm[MM_COUNT];
+};
+
+struct pp_engine {
+  pp_config cfg;
+  int B = 0;             // all slots
+  int ngroups = 1;
+  Group grp[kMaxGroups];
+  Buffers shared;        // per-slot state and staging for all slots (group 0 base)
+  int logits_ld = 0;
+  int dep_priority = 0;  // launch priority of the depformer kernels (higher = more urgent)
   bool tensor = true;
   bool pdl = true;
-  Mm mm[MM_COUNT];
+  cudaStream_t branch[kMaxGroups] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, join[kMaxGroups] = {nullptr, nullptr};
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -107,48 +128,87 @@ struct Carver {
   }
 };
 
-size_t carve(const Dims& D, char* base, Buffers* b) {
+int group_count(const pp_config* c) {
+  return (c->max_batch >= 16 && (c->flags & PP_FLAG_TWO_GROUPS)) ? 2 : 1;
+}
+
+// Workspace layout: per-slot state and staging for all slots first, then each group's
+// ring, activations and operands.  Fills shared and grp[] (pointers) when base != 0.
+size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
   Carver cv{base};
-  const size_t B = D.B;
-  const size_t wide = D.d > D.F ? D.d : D.F;
-  const size_t dwide = D.dd > D.Fd ? D.dd : D.Fd;
-  b->ring = cv.take<uint16_t>((size_t)D.L * B * 2 * D.H * D.W * D.Dh);
-  b->pos = cv.take<int32_t>(B);
-  b->live = cv.take<int32_t>(B);
-  b->ctl = cv.take<int32_t>(B);
-  b->ctl_pos = cv.take<int32_t>(B);
-  b->status = cv.take<uint32_t>(1);
-  b->attn_count = cv.take<uint32_t>(B * D.H);
-  b->in_col = cv.take<int32_t>(B * kRows);
-  b->in_user = cv.take<int32_t>(B * PP_USER_ROWS);
-  b->in_fmask = cv.take<uint8_t>(B * kRows);
-  b->in_forced = cv.take<int32_t>(B * kRows);
-  b->out_col = cv.take<int32_t>(B * kRows);
-  b->x = cv.take<float>(B * D.d);
-  b->xn = cv.take<float>(B * wide);
-  b->z = cv.take<float>(B * D.d);
-  b->qkv = cv.take<float>(B * 3 * D.d);
-  b->q = cv.take<float>(B * D.d);
-  b->o = cv.take<float>(B * D.d);
-  b->hmlp = cv.take<float>(B * D.F);
-  b->rope_cs = cv.take<float>(B * D.Dh);
-  b->attn_part = cv.take<float>(B * D.H * D.nc_max * (D.Dh + 2));
-  b->logits = cv.take<float>(B * D.logits_ld);
-  b->tok = cv.take<int32_t>(B);
-  b->y = cv.take<float>(B * D.dd);
-  b->yn = cv.take<float>(B * dwide);
-  b->dqkv = cv.take<float>(B * 3 * D.dd);
-  b->dkv = cv.take<float>(B * D.Ld * D.nq * 2 * D.dd);
-  b->dout = cv.take<float>(B * D.dd);
-  b->dh = cv.take<float>(B * D.Fd);
-  const size_t R = 2 * (size_t)D.Bp;
-  b->op_d = cv.take<uint16_t>(R * D.d);
-  b->op_o = cv.take<uint16_t>(R * D.d);
-  b->op_f = cv.take<uint16_t>(R * D.F);
-  b->op_z = cv.take<uint16_t>(R * D.d);
-  b->op_dd = cv.take<uint16_t>(R * D.dd);
-  b->op_do = cv.take<uint16_t>(R * D.dd);
-  b->op_fd = cv.take<uint16_t>(R * D.Fd);
+  const size_t B = c->max_batch;
+  const int ng = group_count(c);
+  const size_t ld = (size_t)c->text_vocab + (size_t)c->n_q * c->audio_card;
+  Buffers sh{};
+  sh.pos = cv.take<int32_t>(B);
+  sh.live = cv.take<int32_t>(B);
+  sh.nvalid = cv.take<int32_t>(B);
+  sh.ctl = cv.take<int32_t>(B);
+  sh.ctl_pos = cv.take<int32_t>(B);
+  sh.status = cv.take<uint32_t>(1);
+  sh.in_col = cv.take<int32_t>(B * kRows);
+  sh.in_user = cv.take<int32_t>(B * PP_USER_ROWS);
+  sh.in_fmask = cv.take<uint8_t>(B * kRows);
+  sh.in_forced = cv.take<int32_t>(B * kRows);
+  sh.out_col = cv.take<int32_t>(B * kRows);
+  sh.logits = cv.take<float>(B * ld);
+  if (shared) *shared = sh;
+  int slot0 = 0;
+  for (int g = 0; g < ng; ++g) {
+    const int Bg = (g == 0) ? (int)(B + ng - 1) / ng : (int)B - slot0;
+    pp_config cg = *c;
+    cg.max_batch = Bg;
+    const Dims D = make_dims(&cg);
+    Buffers b = sh;   // per-slot state: this group's slice
+    if (base) {
+      b.pos = sh.pos + slot0;
+      b.live = sh.live + slot0;
+      b.nvalid = sh.nvalid + slot0;
+      b.ctl = sh.ctl + slot0;
+      b.ctl_pos = sh.ctl_pos + slot0;
+      b.in_col = sh.in_col + (size_t)slot0 * kRows;
+      b.in_user = sh.in_user + (size_t)slot0 * PP_USER_ROWS;
+      b.in_fmask = sh.in_fmask + (size_t)slot0 * kRows;
+      b.in_forced = sh.in_forced + (size_t)slot0 * kRows;
+      b.out_col = sh.out_col + (size_t)slot0 * kRows;
+      b.logits = sh.logits + (size_t)slot0 * ld;
+    }
+    const size_t Bs = Bg;
+    const size_t wide = D.d > D.F ? D.d : D.F;
+    const size_t dwide = D.dd > D.Fd ? D.dd : D.Fd;
+    b.ring = cv.take<uint16_t>((size_t)D.L * Bs * 2 * D.H * D.W * D.Dh);
+    b.attn_count = cv.take<uint32_t>(Bs * D.H);
+    b.x = cv.take<float>(Bs * D.d);
+    b.xn = cv.take<float>(Bs * wide);
+    b.z = cv.take<float>(Bs * D.d);
+    b.qkv = cv.take<float>(Bs * 3 * D.d);
+    b.q = cv.take<float>(Bs * D.d);
+    b.o = cv.take<float>(Bs * D.d);
+    b.hmlp = cv.take<float>(Bs * D.F);
+    b.rope_cs = cv.take<float>(Bs * D.Dh);
+    b.attn_part = cv.take<float>(Bs * D.H * D.nc_max * (D.Dh + 2));
+    b.tok = cv.take<int32_t>(Bs);
+    b.y = cv.take<float>(Bs * D.dd);
+    b.yn = cv.take<float>(Bs * dwide);
+    b.dqkv = cv.take<float>(Bs * 3 * D.dd);
+    b.dkv = cv.take<float>(Bs * D.Ld * D.nq * 2 * D.dd);
+    b.dout = cv.take<float>(Bs * D.dd);
+    b.dh = cv.take<float>(Bs * D.Fd);
+    const size_t R = 2 * (size_t)D.Bp;
+    b.op_d = cv.take<uint16_t>(R * D.d);
+    b.op_o = cv.take<uint16_t>(R * D.d);
+    b.op_f = cv.take<uint16_t>(R * D.F);
+    b.op_z = cv.take<uint16_t>(R * D.d);
+    b.op_dd = cv.take<uint16_t>(R * D.dd);
+    b.op_do = cv.take<uint16_t>(R * D.dd);
+    b.op_fd = cv.take<uint16_t>(R * D.Fd);
+    if (grp) {
+      grp[g].slot0 = slot0;
+      grp[g].D = D;
+      grp[g].buf = b;
+    }
+    slot0 += Bg;
+  }
   return (cv.off + 255) & ~(size_t)255;
 }
 
@@ -192,8 +252,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k, uint3
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K-splits per M-tile: a function of the matrix shape and the device's CTA slots only.
-int choose_splits(int m_tiles, int kblocks, int slots) {
+// K-splits per M-tile: a function of the matrix shape and the device's SM count only,
+// never of the batch, so every engine size reduces in the same order.  Model: units run
+// in waves of two CTAs per SM; a unit costs its k-blocks plus a fixed overhead of about
+// three k-blocks (launch share, pipeline fill, epilogue).
+int choose_splits(int m_tiles, int kblocks, int nsm) {
+  const int slots = 2 * nsm;
   int best = 1;
   double best_t = 1e300;
   for (int sp = 1; sp <= kblocks && sp <= kMaxSplits && m_tiles * sp <= kMaxUnits; ++sp) {
@@ -206,34 +270,34 @@ int choose_splits(int m_tiles, int kblocks, int slots) {
 }
 
 bool plan_mm(Mm* g, const void* w, int rows_total, int M, int K, int pair, const uint16_t* op,
-             int Bp, int slots) {
+             int Bp, int nsm) {
   g->M = M;
   g->K = K;
   g->pair = pair;
   g->kblocks = (K + 63) / 64;
   g->m_tiles = pair ? (pair + 63) / 64 : (M + 127) / 128;
   if (g->m_tiles > kMaxTiles) return false;
-  g->splits = choose_splits(g->m_tiles, g->kblocks, slots);
+  g->splits = choose_splits(g->m_tiles, g->kblocks, nsm);
   return make_map(&g->mapA, w, (uint64_t)rows_total, (uint64_t)K, 64) &&
          make_map(&g->mapB, op, (uint64_t)2 * Bp, (uint64_t)K, 2 * Bp);
 }
 
-bool plan_all(pp_engine* e, int slots) {
+bool plan_all(Group* e, int nsm) {
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const int Bp = D.Bp;
   bool ok = true;
-  ok &= plan_mm(&e->mm[MM_QKV], b.wqkv, D.L * 3 * D.d, 3 * D.d, D.d, 0, b.op_d, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_O], b.wo, D.L * D.d, D.d, D.d, 0, b.op_o, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_dd, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_do, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_dd, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DDOWN], b.dep_wdown, D.Ld * D.dd, D.dd, D.Fd, 0, b.op_fd, Bp, slots);
-  ok &= plan_mm(&e->mm[MM_DHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_dd, Bp, slots);
+  ok &= plan_mm(&e->mm[MM_QKV], b.wqkv, D.L * 3 * D.d, 3 * D.d, D.d, 0, b.op_d, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_O], b.wo, D.L * D.d, D.d, D.d, 0, b.op_o, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_dd, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_do, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_dd, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DDOWN], b.dep_wdown, D.Ld * D.dd, D.dd, D.Fd, 0, b.op_fd, Bp, nsm);
+  ok &= plan_mm(&e->mm[MM_DHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_dd, Bp, nsm);
   return ok;
 }
 
@@ -267,7 +331,7 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   } while (0)
 
 // The tick with every weight contraction on the tensor cores.
-cudaError_t enqueue_tick_tensor(const pp_engine* e, cudaStream_t s, Prof* prof) {
+cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s, Prof* prof) {
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
@@ -297,6 +361,7 @@ cudaError_t enqueue_tick_tensor(const pp_engine* e, cudaStream_t s, Prof* prof) 
   PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s));
   MARK(PP_K_TEXT_HEAD);
   PP_TRY(launch_text_argmax(D, b, s));
+  g_launch_priority = dep_priority;   // the latency-bound depformer goes first
   for (int k = 0; k < D.nq; ++k) {
     const uint16_t* emb =
         (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
@@ -435,8 +500,30 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
   return cudaSuccess;
 }
 
+cudaError_t enqueue_group(const pp_engine* e, int g, cudaStream_t s, Prof* prof) {
+  g_launch_priority = 0;
+  cudaError_t err = e->tensor ? enqueue_tick_tensor(&e->grp[g], e->dep_priority, s, prof)
+                              : enqueue_tick_cc(e->grp[g].D, e->grp[g].buf, s, prof);
+  g_launch_priority = 0;
+  return err;
+}
+
+// The whole tick: one branch per slot group (a fork/join inside the captured graph);
+// the profiling graph runs the groups one after the other so that its events time
+// single kernels.
 cudaError_t enqueue_tick(const pp_engine* e, cudaStream_t s, Prof* prof) {
-  return e->tensor ? enqueue_tick_tensor(e, s, prof) : enqueue_tick_cc(e->D, e->buf, s, prof);
+  if (e->ngroups == 1 || prof) {
+    for (int g = 0; g < e->ngroups; ++g) PP_TRY(enqueue_group(e, g, s, prof));
+    return cudaSuccess;
+  }
+  PP_TRY(cudaEventRecord(e->fork, s));
+  for (int g = 0; g < e->ngroups; ++g) {
+    PP_TRY(cudaStreamWaitEvent(e->branch[g], e->fork, 0));
+    PP_TRY(enqueue_group(e, g, e->branch[g], nullptr));
+    PP_TRY(cudaEventRecord(e->join[g], e->branch[g]));
+    PP_TRY(cudaStreamWaitEvent(s, e->join[g], 0));
+  }
+  return cudaSuccess;
 }
 
 int weight_dims(const pp_config* c, int which, int64_t d[4], int* nd, int* f32) {
@@ -485,8 +572,7 @@ int pp_weight_shape(const pp_config* c, int which, int64_t dims[4], int* ndim, i
 
 size_t pp_workspace_bytes(const pp_config* c) {
   if (!config_ok(c)) return 0;
-  Buffers b{};
-  return carve(make_dims(c), nullptr, &b);
+  return carve(c, nullptr, nullptr, nullptr);
 }
 
 int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t ws_bytes,
@@ -497,61 +583,83 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return PP_EINVAL;
   for (int i = 0; i < PP_W_COUNT; ++i)
     if (!w->ptr[i] || (reinterpret_cast<uintptr_t>(w->ptr[i]) & 15)) return PP_EINVAL;
-  const Dims D = make_dims(c);
-  Buffers b{};
-  const size_t need = carve(D, reinterpret_cast<char*>(workspace), &b);
-  if (ws_bytes < need) return PP_E_NOSPACE;
-  b.emb_text = (const uint16_t*)w->ptr[PP_W_EMB_TEXT];
-  b.emb_audio = (const uint16_t*)w->ptr[PP_W_EMB_AUDIO];
-  b.attn_alpha = (const float*)w->ptr[PP_W_ATTN_ALPHA];
-  b.wqkv = (const uint16_t*)w->ptr[PP_W_QKV];
-  b.wo = (const uint16_t*)w->ptr[PP_W_O];
-  b.mlp_alpha = (const float*)w->ptr[PP_W_MLP_ALPHA];
-  b.wgu = (const uint16_t*)w->ptr[PP_W_GU];
-  b.wdown = (const uint16_t*)w->ptr[PP_W_DOWN];
-  b.out_alpha = (const float*)w->ptr[PP_W_OUT_ALPHA];
-  b.wtext = (const uint16_t*)w->ptr[PP_W_TEXT];
-  b.dep_inproj = (const uint16_t*)w->ptr[PP_W_DEP_INPROJ];
-  b.dep_emb_text = (const uint16_t*)w->ptr[PP_W_DEP_EMB_TEXT];
-  b.dep_emb_audio = (const uint16_t*)w->ptr[PP_W_DEP_EMB_AUDIO];
-  b.dep_attn_alpha = (const float*)w->ptr[PP_W_DEP_ATTN_ALPHA];
-  b.dep_wqkv = (const uint16_t*)w->ptr[PP_W_DEP_QKV];
-  b.dep_wo = (const uint16_t*)w->ptr[PP_W_DEP_O];
-  b.dep_mlp_alpha = (const float*)w->ptr[PP_W_DEP_MLP_ALPHA];
-  b.dep_wgu = (const uint16_t*)w->ptr[PP_W_DEP_GU];
-  b.dep_wdown = (const uint16_t*)w->ptr[PP_W_DEP_DOWN];
-  b.dep_out_alpha = (const float*)w->ptr[PP_W_DEP_OUT_ALPHA];
-  b.dep_heads = (const uint16_t*)w->ptr[PP_W_DEP_HEADS];
-
   pp_engine* e = new (std::nothrow) pp_engine();
   if (!e) return PP_EINVAL;
+  const size_t need = carve(c, reinterpret_cast<char*>(workspace), &e->shared, e->grp);
+  if (ws_bytes < need) {
+    delete e;
+    return PP_E_NOSPACE;
+  }
   e->cfg = *c;
-  e->D = D;
-  e->buf = b;
-  e->ctl.assign(D.B, 0);
-  e->ctl_pos.assign(D.B, 0);
-  e->pos.assign(D.B, 0);
-  e->open.assign(D.B, 0);
+  e->B = c->max_batch;
+  e->ngroups = group_count(c);
+  e->logits_ld = c->text_vocab + c->n_q * c->audio_card;
+  for (int g = 0; g < e->ngroups; ++g) {
+    Buffers& b = e->grp[g].buf;
+    b.emb_text = (const uint16_t*)w->ptr[PP_W_EMB_TEXT];
+    b.emb_audio = (const uint16_t*)w->ptr[PP_W_EMB_AUDIO];
+    b.attn_alpha = (const float*)w->ptr[PP_W_ATTN_ALPHA];
+    b.wqkv = (const uint16_t*)w->ptr[PP_W_QKV];
+    b.wo = (const uint16_t*)w->ptr[PP_W_O];
+    b.mlp_alpha = (const float*)w->ptr[PP_W_MLP_ALPHA];
+    b.wgu = (const uint16_t*)w->ptr[PP_W_GU];
+    b.wdown = (const uint16_t*)w->ptr[PP_W_DOWN];
+    b.out_alpha = (const float*)w->ptr[PP_W_OUT_ALPHA];
+    b.wtext = (const uint16_t*)w->ptr[PP_W_TEXT];
+    b.dep_inproj = (const uint16_t*)w->ptr[PP_W_DEP_INPROJ];
+    b.dep_emb_text = (const uint16_t*)w->ptr[PP_W_DEP_EMB_TEXT];
+    b.dep_emb_audio = (const uint16_t*)w->ptr[PP_W_DEP_EMB_AUDIO];
+    b.dep_attn_alpha = (const float*)w->ptr[PP_W_DEP_ATTN_ALPHA];
+    b.dep_wqkv = (const uint16_t*)w->ptr[PP_W_DEP_QKV];
+    b.dep_wo = (const uint16_t*)w->ptr[PP_W_DEP_O];
+    b.dep_mlp_alpha = (const float*)w->ptr[PP_W_DEP_MLP_ALPHA];
+    b.dep_wgu = (const uint16_t*)w->ptr[PP_W_DEP_GU];
+    b.dep_wdown = (const uint16_t*)w->ptr[PP_W_DEP_DOWN];
+    b.dep_out_alpha = (const float*)w->ptr[PP_W_DEP_OUT_ALPHA];
+    b.dep_heads = (const uint16_t*)w->ptr[PP_W_DEP_HEADS];
+  }
+  e->ctl.assign(e->B, 0);
+  e->ctl_pos.assign(e->B, 0);
+  e->pos.assign(e->B, 0);
+  e->open.assign(e->B, 0);
 
   e->tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
   g_use_pdl = (c->flags & PP_FLAG_PDL) != 0;   // read while this engine's graphs are captured
   cudaError_t err = cudaSuccess;
-  // zero the small state (positions, liveness, control, status, attention counters)
-  char* small_lo = reinterpret_cast<char*>(b.pos);
-  char* small_hi = reinterpret_cast<char*>(b.in_col);
-  err = cudaMemset(small_lo, 0, (size_t)(small_hi - small_lo));
-  if (err == cudaSuccess) {   // operands: their padding rows stay zero
-    char* op_lo = reinterpret_cast<char*>(b.op_d);
-    char* op_hi = reinterpret_cast<char*>(b.op_fd + 2 * (size_t)D.Bp * D.Fd);
-    err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
+  {  // zero the per-slot state (positions, liveness, control, status)
+    const Buffers& sh = e->shared;
+    err = cudaMemset(sh.pos, 0, (size_t)(reinterpret_cast<char*>(sh.in_col) -
+                                          reinterpret_cast<char*>(sh.pos)));
+  }
+  for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+    const Buffers& b = e->grp[g].buf;
+    const Dims& D = e->grp[g].D;
+    err = cudaMemset(b.attn_count, 0, sizeof(uint32_t) * (size_t)D.B * D.H);
+    if (err == cudaSuccess) {   // operands: their padding rows stay zero
+      char* op_lo = reinterpret_cast<char*>(b.op_d);
+      char* op_hi = reinterpret_cast<char*>(b.op_fd + 2 * (size_t)D.Bp * D.Fd);
+      err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
+    }
   }
   if (err == cudaSuccess && e->tensor) {
     int dev = 0, nsm = 0;
     err = cudaGetDevice(&dev);
     if (err == cudaSuccess)
       err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = umma_setup(2 * D.Bp);
-    if (err == cudaSuccess && !plan_all(e, 2 * nsm)) err = cudaErrorInvalidValue;
+    for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+      err = umma_setup(2 * e->grp[g].D.Bp);
+      if (err == cudaSuccess && !plan_all(&e->grp[g], nsm)) err = cudaErrorInvalidValue;
+    }
+  }
+  if (err == cudaSuccess && e->ngroups > 1) {
+    int least = 0, greatest = 0;
+    err = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    e->dep_priority = greatest;
+    for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+      err = cudaStreamCreateWithFlags(&e->branch[g], cudaStreamNonBlocking);
+      if (err == cudaSuccess) err = cudaEventCreateWithFlags(&e->join[g], cudaEventDisableTiming);
+    }
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&e->fork, cudaEventDisableTiming);
   }
   if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&e->cap_stream, cudaStreamNonBlocking);
   e->pdl = g_use_pdl;
@@ -585,12 +693,17 @@ void pp_destroy(pp_engine* e) {
   if (e->exec) cudaGraphExecDestroy(e->exec);
   if (e->graph) cudaGraphDestroy(e->graph);
   if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
+  for (int g = 0; g < kMaxGroups; ++g) {
+    if (e->branch[g]) cudaStreamDestroy(e->branch[g]);
+    if (e->join[g]) cudaEventDestroy(e->join[g]);
+  }
+  if (e->fork) cudaEventDestroy(e->fork);
   delete e;
 }
 
 static int open_at(pp_engine* e, int slot, int64_t pos) {
   if (!e) return PP_EINVAL;
-  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (slot < 0 || slot >= e->B) return PP_E_RANGE;
   if (pos < 0 || pos >= 0x7FFFFFFF) return PP_E_RANGE;
   if (e->open[slot]) return PP_E_BUSY;
   e->open[slot] = 1;
@@ -607,7 +720,7 @@ int pp_session_import(pp_engine* e, int slot, int64_t pos) { return open_at(e, s
 
 int pp_session_close(pp_engine* e, int slot) {
   if (!e) return PP_EINVAL;
-  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (slot < 0 || slot >= e->B) return PP_E_RANGE;
   if (!e->open[slot]) return PP_E_NOTLIVE;
   e->open[slot] = 0;
   e->ctl[slot] = 0;
@@ -617,7 +730,7 @@ int pp_session_close(pp_engine* e, int slot) {
 
 int pp_session_pos(pp_engine* e, int slot, int64_t* pos) {
   if (!e || !pos) return PP_EINVAL;
-  if (slot < 0 || slot >= e->D.B) return PP_E_RANGE;
+  if (slot < 0 || slot >= e->B) return PP_E_RANGE;
   if (!e->open[slot]) return PP_E_NOTLIVE;
   *pos = e->pos[slot];
   return PP_OK;
@@ -625,9 +738,12 @@ int pp_session_pos(pp_engine* e, int slot, int64_t* pos) {
 
 int pp_ring_block(pp_engine* e, int layer, int slot, int kv, void** ptr) {
   if (!e || !ptr || (kv != 0 && kv != 1)) return PP_EINVAL;
-  if (layer < 0 || layer >= e->D.L || slot < 0 || slot >= e->D.B) return PP_E_RANGE;
-  const Dims& D = e->D;
-  *ptr = e->buf.ring + ((((size_t)layer * D.B + slot) * 2 + kv) * D.H) * (size_t)D.W * D.Dh;
+  if (layer < 0 || layer >= e->grp[0].D.L || slot < 0 || slot >= e->B) return PP_E_RANGE;
+  int g = e->ngroups - 1;
+  while (slot < e->grp[g].slot0) --g;
+  const Dims& D = e->grp[g].D;
+  const int s = slot - e->grp[g].slot0;
+  *ptr = e->grp[g].buf.ring + ((((size_t)layer * D.B + s) * 2 + kv) * D.H) * (size_t)D.W * D.Dh;
   return PP_OK;
 }
 
@@ -636,9 +752,8 @@ static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* us
                      float* logits, cudaStream_t s, bool wait, cudaGraphExec_t exec) {
   if (!e || !prev_column || !user_codes || !column) return PP_EINVAL;
   if ((force_mask != nullptr) != (forced_tokens != nullptr)) return PP_EINVAL;
-  const Dims& D = e->D;
-  const Buffers& b = e->buf;
-  const size_t B = D.B;
+  const Buffers& b = e->shared;
+  const size_t B = e->B;
   cudaError_t err = cudaMemcpyAsync(b.in_col, prev_column, B * kRows * 4, cudaMemcpyDefault, s);
   if (err == cudaSuccess)
     err = cudaMemcpyAsync(b.in_user, user_codes, B * PP_USER_ROWS * 4, cudaMemcpyDefault, s);
@@ -662,7 +777,7 @@ static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* us
   if (err == cudaSuccess)
     err = cudaMemcpyAsync(column, b.out_col, B * kRows * 4, cudaMemcpyDefault, s);
   if (err == cudaSuccess && logits)
-    err = cudaMemcpyAsync(logits, b.logits, B * (size_t)D.logits_ld * 4, cudaMemcpyDefault, s);
+    err = cudaMemcpyAsync(logits, b.logits, B * (size_t)e->logits_ld * 4, cudaMemcpyDefault, s);
   if (err == cudaSuccess && wait) err = cudaStreamSynchronize(s);
   if (err != cudaSuccess) return PP_E_CUDA;
   if (upload) {
@@ -732,8 +847,8 @@ int pp_status(pp_engine* e, void* stream, uint32_t* bits) {
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t v = 0;
   cudaError_t err = cudaStreamSynchronize(s);
-  if (err == cudaSuccess) err = cudaMemcpy(&v, e->buf.status, 4, cudaMemcpyDeviceToHost);
-  if (err == cudaSuccess) err = cudaMemset(e->buf.status, 0, 4);
+  if (err == cudaSuccess) err = cudaMemcpy(&v, e->shared.status, 4, cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess) err = cudaMemset(e->shared.status, 0, 4);
   if (err == cudaSuccess) err = cudaDeviceSynchronize();
   if (err != cudaSuccess) return PP_E_CUDA;
   *bits = v;
@@ -741,5 +856,53 @@ int pp_status(pp_engine* e, void* stream, uint32_t* bits) {
 }
 
 int pp_step_kernel_count(pp_engine* e) { return e ? e->n_kernels : PP_EINVAL; }
+
+static bool ring_attention_args_ok(int B, int H, int head_dim, int window) {
+  return B >= 1 && H >= 1 && window >= 1 && head_dim_ok(head_dim) &&
+         (int64_t)B * H <= (int64_t)1 << 24 && window <= (1 << 24);
+}
+
+static size_t ring_attention_part_bytes(int B, int H, int head_dim, int window) {
+  const size_t nc = (size_t)(window + kAttnChunk - 1) / kAttnChunk;
+  return (((size_t)B * H * nc * (head_dim + 2) * sizeof(float)) + 255) & ~(size_t)255;
+}
+
+size_t pp_ring_attention_scratch_bytes(int B, int H, int head_dim, int window) {
+  if (!ring_attention_args_ok(B, H, head_dim, window)) return 0;
+  return ring_attention_part_bytes(B, H, head_dim, window) + (size_t)B * H * sizeof(uint32_t);
+}
+
+int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int64_t slot_stride,
+                      const int32_t* n_valid, int B, int H, int head_dim, int window,
+                      float* out, void* scratch, size_t scratch_bytes, void* stream) {
+  if (!ring_attention_args_ok(B, H, head_dim, window)) return PP_EINVAL;
+  if (!q || !k || !v || !n_valid || !out || !scratch || slot_stride < 0) return PP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v)) & 15)
+    return PP_EINVAL;
+  if ((slot_stride & 7) || (reinterpret_cast<uintptr_t>(scratch) & 255)) return PP_EINVAL;
+  if (scratch_bytes < pp_ring_attention_scratch_bytes(B, H, head_dim, window)) return PP_E_NOSPACE;
+  AttnArgs a{};
+  a.q = q;
+  a.q_ld = H * head_dim;
+  a.q_scale = 1.4426950408889634f / sqrtf((float)head_dim);
+  a.k = k;
+  a.v = v;
+  a.slot_stride = (size_t)slot_stride;
+  a.n_valid = n_valid;
+  a.H = H;
+  a.W = window;
+  a.nc_max = (window + kAttnChunk - 1) / kAttnChunk;
+  a.out = out;
+  a.out_ld = H * head_dim;
+  a.op = nullptr;
+  a.part = reinterpret_cast<float*>(scratch);
+  a.count = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(scratch) +
+                                        ring_attention_part_bytes(B, H, head_dim, window));
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t err = cudaMemsetAsync(a.count, 0, (size_t)B * H * sizeof(uint32_t), s);
+  if (err == cudaSuccess) err = launch_attn_args(a, B, head_dim, s);
+  return err == cudaSuccess ? PP_OK : PP_E_CUDA;
+}
 
 }  // extern "C"

@@ -49,6 +49,7 @@ struct Buffers {
   uint16_t* ring;          // [L][B][2][H][W][Dh] bf16
   int32_t* pos;            // [B]
   int32_t* live;           // [B]
+  int32_t* nvalid;         // [B] valid ring positions this tick (0 = closed slot)
   int32_t* ctl;            // [B] host-uploaded control: bit0 live, bit1 reset position
   int32_t* ctl_pos;        // [B] position applied when bit1 is set
   uint32_t* status;        // [1]
@@ -101,7 +102,8 @@ __device__ __forceinline__ void pdl_wait_and_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-extern bool g_use_pdl;   // set by the engine before it captures a tick
+extern bool g_use_pdl;          // set by the engine before it captures a tick
+extern int g_launch_priority;    // nonzero: launch priority attribute of the next launches
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
@@ -111,8 +113,13 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   int n = 0;
+  if (g_launch_priority != 0) {
+    at[n].id = cudaLaunchAttributePriority;
+    at[n].val.priority = g_launch_priority;
+    ++n;
+  }
   if (g_use_pdl) {
     at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[n].val.programmaticStreamSerializationAllowed = 1;
@@ -187,6 +194,25 @@ struct GemvArgs {
 cudaError_t launch_gemv(const Dims& D, const GemvArgs& a, cudaStream_t s);
 
 cudaError_t launch_rope_ring(const Dims& D, const Buffers& b, int layer, cudaStream_t s);
+// Split-K ring attention (k_attn.cu): for slot s < B and head h < H,
+//   out[s][h*Dh + i] = sum_j softmax_j(q_scale * q.K_j, base 2) V_j,  j < n_valid[s].
+struct AttnArgs {
+  const float* q;          // [B][q_ld], head h at h*Dh
+  int q_ld;
+  float q_scale;           // multiplies q; log2(e)/sqrt(Dh) for a plain softmax
+  const uint16_t* k;       // head h of slot s: k + s*slot_stride + h*W*Dh, [W][Dh] bf16
+  const uint16_t* v;
+  size_t slot_stride;      // elements
+  const int32_t* n_valid;  // [B]; values above W count as W, values <= 0 give zero output
+  int H, W, nc_max;        // nc_max = ceil(W / kAttnChunk)
+  float* out;              // [B][out_ld] fp32
+  int out_ld;
+  uint16_t* op;            // optional bf16 hi/lo operand [2*op_Bp][H*Dh]
+  int op_Bp;
+  float* part;             // scratch [B*H][nc_max][Dh+2]
+  uint32_t* count;         // scratch [B*H], zero before the call; left zero after it
+};
+cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, cudaStream_t s);
 cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s);
 cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,

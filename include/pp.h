@@ -82,6 +82,12 @@ typedef struct {
  * while its predecessor drains and waits for it in-kernel).  Off by default: on GB300
  * the tick measured faster without it. */
 #define PP_FLAG_PDL 0x2
+/* Split an engine of 16 or more slots into two groups that run as parallel branches of
+ * the tick graph, so one group's latency-bound depformer can overlap the other's
+ * bandwidth-bound attention (weights are then streamed once per group).  Off by
+ * default: on GB300 the doubled weight traffic cost more than the overlap saved.
+ * Grouping never changes a session's bits. */
+#define PP_FLAG_TWO_GROUPS 0x4
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */
@@ -218,6 +224,28 @@ enum pp_kernel_kind {
 int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
                     const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
                     float* logits, void* stream, double* kind_ms, int64_t* kind_launches);
+
+/* ---- the tick's attention as a standalone call ---------------------------------------
+ * Split-K sliding-window decode attention over ring blocks, the kernel each layer of
+ * pp_step runs (vllm-omni recipe, "Architecture": a 3000-frame sliding window held in a
+ * ring KV cache per slot).  For slot s < B and head h < H:
+ *   out[s][h*D + i] = sum_{j < n_valid[s]} softmax_j(q[s][h] . K_j / sqrt(D)) V_j[i]
+ * over ring indices j (softmax does not depend on key order, so the ring need not be
+ * rotated); n_valid[s] == 0 gives zeros.  Reductions run in a fixed order set by the
+ * ring index alone, so every slot's result is independent of the others.
+ *   q          f32 [B][H][D], device, 16-byte aligned
+ *   k, v       bf16: head h of slot s is the [W][D] block at k + s*slot_stride + h*W*D
+ *              (elements), device, 16-byte aligned, slot_stride a multiple of 8
+ *   n_valid    int32 [B], device; values above W count as W, values <= 0 give zeros
+ *   out        f32 [B][H*D], device
+ *   scratch    device memory of at least pp_ring_attention_scratch_bytes(B, H, D, W)
+ *              bytes, 256-byte aligned, caller-owned; its contents need no set-up
+ * D (head_dim) is 32, 64 or 128.  Asynchronous on `stream`.  Errors: PP_EINVAL,
+ * PP_E_NOSPACE (scratch too small), PP_E_CUDA. */
+size_t pp_ring_attention_scratch_bytes(int B, int H, int head_dim, int window);
+int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int64_t slot_stride,
+                      const int32_t* n_valid, int B, int H, int head_dim, int window,
+                      float* out, void* scratch, size_t scratch_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -46,6 +46,8 @@ class Placement:
     slot: int
     start: int          # global tick at which the session opens
     script: Script      # it runs script.T ticks, then closes
+    import_pos: int = -1     # >= 0: resume at this position (ring already filled)
+    check: bool = True       # False: run on the GPU only (a neighbour, not compared)
 
 
 def device_weights(w_host, device="cuda"):
@@ -60,10 +62,11 @@ def device_weights(w_host, device="cuda"):
 
 
 def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=None,
-               oracle_sessions=None, flags=0):
+               oracle_sessions=None, flags=0, setup=None):
     """Run the placements on a GPU engine of B slots with teacher forcing against the
     oracle; asserts column equality and the logit tolerance every tick.  Returns a dict
-    of statistics."""
+    of statistics.  setup(engine), if given, runs once before the first tick (e.g. to
+    fill imported sessions' rings)."""
     import torch
 
     import full_duplex_speech_lockstep_gb300 as pp
@@ -71,6 +74,8 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
 
     orc = oracle.Oracle(shape, w_host)
     eng = pp.Engine(shape, B, w_dev, flags=flags)
+    if setup is not None:
+        setup(eng)
     T_end = max(p.start + p.script.T for p in placements)
     Vt, Va, nq = shape.text_vocab, shape.audio_card, shape.n_q
     ld = Vt + nq * Va
@@ -83,9 +88,16 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
                 eng.close(p.slot)
                 del sess[p.slot]
             if p.start == t:
-                eng.open(p.slot)
+                if p.import_pos >= 0:
+                    eng.import_session(p.slot, p.import_pos)
+                else:
+                    eng.open(p.slot)
                 o = (oracle_sessions or {}).get(p.slot)
-                sess[p.slot] = [p, orc.new_session() if o is None else o, initial_column(shape)]
+                if not p.check:
+                    o = None
+                elif o is None:
+                    o = orc.new_session()
+                sess[p.slot] = [p, o, initial_column(shape)]
         prev = np.tile(initial_column(shape), (B, 1))
         user = np.zeros((B, 8), np.int32)
         fmask = np.zeros((B, ROWS), np.uint8)
@@ -94,6 +106,12 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
         for slot, (p, os_, pcol) in sess.items():
             i = t - p.start
             sc = p.script
+            if os_ is None:     # unchecked neighbour: free-running on the GPU
+                prev[slot] = pcol
+                user[slot] = sc.user[i]
+                fmask[slot] = sc.fmask[i]
+                forced[slot] = sc.forced[i]
+                continue
             col, lt, la = orc.step(os_, pcol, sc.user[i], sc.fmask[i], sc.forced[i])
             expect[slot] = (col, lt, la)
             prev[slot] = pcol
@@ -117,6 +135,9 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
         colg = colg.cpu().numpy()
         lg = logits_dev.cpu().numpy() if check_logits else None
         for slot in range(B):
+            if slot in sess and slot not in expect:
+                sess[slot][2] = colg[slot].copy()
+                continue
             if slot not in expect:
                 assert np.all(colg[slot] == -1), (t, slot, colg[slot])
                 continue

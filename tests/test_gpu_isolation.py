@@ -54,9 +54,14 @@ def _run(eng, B, shape, sessions, T_end, want_logits=True):
     return out
 
 
-def _check_isolation(shape, B, sessions, T_end, w_dev):
+def pp_flags_two_groups():
     import full_duplex_speech_lockstep_gb300 as pp
-    eng = pp.Engine(shape, B, w_dev)
+    return pp.PP_FLAG_TWO_GROUPS
+
+
+def _check_isolation(shape, B, sessions, T_end, w_dev, flags=0):
+    import full_duplex_speech_lockstep_gb300 as pp
+    eng = pp.Engine(shape, B, w_dev, flags=flags)
     batched = _run(eng, B, shape, sessions, T_end)
     assert eng.status() == 0
     eng.close_engine()
@@ -71,13 +76,33 @@ def _check_isolation(shape, B, sessions, T_end, w_dev):
 
 
 def test_elastic_isolation_small():
-    """B=12 (two operand groups of 8) with joins, leaves and recycled slots."""
+    """B=18 (two slot groups of 9, ragged operand padding) with joins, leaves and
+    recycled slots."""
     s = synth.SMALL
     w = synth.make_weights_host(s, 11, alpha="random")
-    sessions = schedules.elastic_schedule(s, 3, n_slots=12, T=120, initial=6, mean_gap=6,
+    sessions = schedules.elastic_schedule(s, 3, n_slots=18, T=120, initial=9, mean_gap=5,
                                           prefill=(8, 30))
-    assert len(sessions) > 12
-    _check_isolation(s, 12, sessions, 120, device_weights(w))
+    assert len(sessions) > 18
+    _check_isolation(s, 18, sessions, 120, device_weights(w), flags=pp_flags_two_groups())
+
+
+def test_grouping_does_not_change_bits():
+    """The same sessions in a two-group engine and a one-group engine: bit-identical."""
+    import full_duplex_speech_lockstep_gb300 as pp
+    s = synth.TINY
+    w = device_weights(synth.make_weights_host(s, 13, alpha="random"))
+    sessions = []
+    for i in range(20):
+        user, fm, fo = schedules.prefill_session(s, 200 + i, T=15, voice=2, persona=3)
+        sessions.append((i, i % 3, user, fm, fo))
+    outs = []
+    for flags in [0, pp.PP_FLAG_TWO_GROUPS]:
+        e = pp.Engine(s, 20, w, flags=flags)
+        outs.append(_run(e, 20, s, sessions, 18))
+        e.close_engine()
+    for i in range(len(sessions)):
+        assert np.array_equal(np.array(outs[0][i][0]), np.array(outs[1][i][0]))
+        assert np.array_equal(np.array(outs[0][i][1]).view(np.uint32), np.array(outs[1][i][1]).view(np.uint32))
 
 
 def test_isolation_across_engine_sizes():
