@@ -35,7 +35,8 @@ PP_W_COUNT = len(WEIGHT_NAMES)
 EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_session_open", "pp_session_close", "pp_session_import", "pp_session_pos",
            "pp_ring_block", "pp_step", "pp_step_host", "pp_status", "pp_step_kernel_count",
-           "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention"]
+           "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention",
+           "pp_ring_attention_noalloc"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -108,6 +109,8 @@ def lib():
         L.pp_ring_attention_scratch_bytes.restype = ctypes.c_size_t
         L.pp_ring_attention.argtypes = [P, P, P, I64, P, I, I, I, I, P, P, ctypes.c_size_t, P]
         L.pp_ring_attention.restype = I
+        L.pp_ring_attention_noalloc.argtypes = [P, P, P, I64, P, I, I, I, I, P, P]
+        L.pp_ring_attention_noalloc.restype = I
         _lib = L
     return _lib
 
@@ -221,6 +224,13 @@ def pp_ring_attention(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out
     return _check("pp_ring_attention", lib().pp_ring_attention(
         q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, scratch, scratch_bytes,
         stream))
+
+
+def pp_ring_attention_noalloc(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out,
+                              stream):
+    """pp_ring_attention with the library's built-in scratch (no allocation)."""
+    return _check("pp_ring_attention_noalloc", lib().pp_ring_attention_noalloc(
+        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, stream))
 
 
 # ---- convenience wrapper over torch device memory ---------------------------------------

@@ -247,6 +247,23 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
                       const int32_t* n_valid, int B, int H, int head_dim, int window,
                       float* out, void* scratch, size_t scratch_bytes, void* stream);
 
+/* pp_ring_attention for callers that cannot allocate device memory or pass scratch:
+ * for example a host whose device memory all belongs to a pooling allocator that a
+ * library must not bypass or grow, or a real-time frame loop in which an allocation
+ * (it can synchronise the device and take milliseconds) would break the 80 ms cadence.
+ * The pages have no counterpart to this call; it exists for those callers.
+ * Same arguments and result as pp_ring_attention, minus the scratch: the partials and
+ * tickets live in one device array built into the library (about 12.2 MiB, held on
+ * every GPU that loads the library until the process exits).  Limits: B*H <= 2048,
+ * window <= 3072, head_dim <= 128; larger sizes return PP_E_RANGE.  The first call on
+ * a device looks up the array's device address (make that first call before any
+ * stream capture).  Every call shares the array, so calls that overlap on the GPU
+ * (other streams, other threads) race; each call resets the tickets it needs.
+ * Allocates no memory.  Errors: PP_EINVAL, PP_E_RANGE, PP_E_CUDA. */
+int pp_ring_attention_noalloc(const float* q, const uint16_t* k, const uint16_t* v,
+                              int64_t slot_stride, const int32_t* n_valid, int B, int H,
+                              int head_dim, int window, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
