@@ -1,0 +1,76 @@
+"""Parity at the full PersonaPlex shape (GPU): the B=1 prefill workload teacher-forced
+against the oracle, and the bench's launch configuration (64 slots, every ring full at
+3000 positions) with sampled slots checked against the oracle."""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from synth import schedules
+from harness import Placement, Script, greedy_script, run_parity
+
+pytestmark = pytest.mark.gpu
+FULL = synth.FULL
+SEED = 1
+TICKS = int(os.environ.get("PP_FULL_TICKS", "40"))   # 250 runs the whole prefill workload
+
+
+@pytest.fixture(scope="module")
+def full_weights():
+    w_dev = synth.make_weights_device(FULL, SEED)
+    w_host = synth.make_weights_host(FULL, SEED)
+    return w_host, w_dev
+
+
+def test_device_generator_matches_host(full_weights):
+    """The device-generated weights are the host generator's bits (sampled)."""
+    w_host, w_dev = full_weights
+    rng = np.random.default_rng(0)
+    for name, h in w_host.items():
+        d = w_dev[name].reshape(-1)
+        hf = h.reshape(-1)
+        idx = rng.integers(0, hf.size, 4096)
+        got = d[idx].cpu().numpy()
+        if h.dtype == np.uint16:
+            got = got.view(np.uint16)
+        assert np.array_equal(got, hf[idx]), name
+
+
+def test_full_b1_prefill_parity(full_weights):
+    """Voice prefill, silence, persona text: teacher-forced, every tick."""
+    w_host, w_dev = full_weights
+    user, fm, fo = schedules.prefill_session(FULL, SEED, T=TICKS)
+    st = run_parity(FULL, 1, w_host, w_dev, [Placement(0, 0, Script(user, fm, fo))])
+    print("full b1", st)
+    assert st["status"] == 0 and st["ticks"] == TICKS
+
+
+def test_full_b64_full_ring_sampled(full_weights):
+    """64 slots resumed at position 3000 with seeded N(0,1) rings (the bench workload);
+    slots 0, 37 and 63 are checked against the oracle on the same rings."""
+    import oracle
+    w_host, w_dev = full_weights
+    L, W = FULL.n_layers, FULL.window
+    checked = [0, 37, 63]
+    ora = {}
+    for s in checked:
+        rk = np.stack([synth.ring_kv_host(FULL, SEED, s, l, 0) for l in range(L)])
+        rv = np.stack([synth.ring_kv_host(FULL, SEED, s, l, 1) for l in range(L)])
+        ora[s] = oracle.Session(FULL, pos=W, ring_k=rk, ring_v=rv)
+
+    def setup(eng):
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+        for s in range(64):
+            for l in range(L):
+                for kv in range(2):
+                    synth.ring_kv_fill_device(eng.ring_block(l, s, kv), FULL, SEED, s, l, kv,
+                                              stream)
+        torch.cuda.synchronize()
+
+    pl = [Placement(s, 0, greedy_script(FULL, 2, 50 + s), import_pos=W, check=s in checked)
+          for s in range(64)]
+    st = run_parity(FULL, 64, w_host, w_dev, pl, oracle_sessions=ora, setup=setup)
+    print("full b64", st)
+    assert st["status"] == 0
