@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 4) k_attn(AttnArgs a) {
   }
   __threadfence();
   __syncthreads();
+  pdl_trigger();   // this chunk is done: the next kernel may start launching
   if (threadIdx.x == 0) {
     const unsigned prev = atomicAdd(a.count + (size_t)s * a.H + h, 1u);
     sm_last = (prev == (unsigned)(nc - 1));

@@ -51,7 +51,8 @@ __device__ __forceinline__ float block_sum(float v, float* sh) {
 // One CTA per slot.  Applies the host's control word (open/close/reset position),
 // validates the previous column, sums its 17 embedding rows in fp32 in row order
 // (text row first), and tabulates cos/sin of this frame's RoPE angles from fp64.
-__global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
+__global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b, const float* alpha,
+                                              uint16_t* op, float* ssq) {
   pdl_wait_and_trigger();
   const int s = blockIdx.x;
   __shared__ int col[kRows];
@@ -97,6 +98,18 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
     }
     reinterpret_cast<float4*>(x + i)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     reinterpret_cast<float4*>(x + i)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (op) {   // the first layer's fused RMSNorm: operand hi/lo(alpha * x)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) op_store(op, D.d, D.Bp, s, i + t, alpha[i + t] * acc[t]);
+    }
+  }
+  if (op) {   // and the sum of x^2 (fixed order: per thread, then per warp, then warps)
+    __shared__ float sh[9];
+    __syncthreads();
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < D.d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+    ss = block_sum<256>(ss, sh);
+    if (threadIdx.x == 0) ssq[s] = ss;
   }
   // RoPE angles pos * base^(-2i/Dh), evaluated in fp64 and rounded once to fp32
   for (int i = threadIdx.x; i < D.Dh / 2; i += blockDim.x) {
@@ -109,8 +122,9 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b) {
   }
 }
 
-cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s) {
-  { cudaError_t e_ = launch_k(k_begin, dim3(D.B), dim3(256), 0, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
+cudaError_t launch_begin(const Dims& D, const Buffers& b, const float* alpha, uint16_t* op,
+                         float* ssq, cudaStream_t s) {
+  { cudaError_t e_ = launch_k(k_begin, dim3(D.B), dim3(256), 0, s, 1, D, b, alpha, op, ssq); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 

@@ -152,7 +152,7 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (96 * 1024) / kStageBytes < 8 ? (96 * 1024) / kStageBytes : 8;
   static constexpr int kTmemCols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
-  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, 1/rms*/;
 };
 
 template <int N>
@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(128, 2)
   // bars[0..S) full, bars[S..2S) empty, bars[2S] done; then the TMEM address and flags
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_rstd = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + 256);  // [B]
+  const bool norm_in = a.ssq_in != nullptr || a.rstd_in != nullptr;
+  const bool norm_out = a.norm_alpha != nullptr;
 
   pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -248,12 +251,29 @@ __global__ void __launch_bounds__(128, 2)
       umma_commit(smem_u32(&bars[C::kStages + s]));
     }
     umma_commit(smem_u32(&bars[2 * C::kStages]));
+  } else if (warp >= 2 && norm_in) {
+    // fused RMSNorm of the input: 1/rms of every slot, summed from the producer's
+    // partials in slice order while the main loop runs
+    for (int b = threadIdx.x - 64; b < a.B; b += 64) {
+      float rs;
+      if (a.rstd_in) {
+        rs = a.rstd_in[b];
+      } else {
+        float ss = 0.f;
+#pragma unroll 8
+        for (int q = 0; q < a.ssq_nparts; ++q) ss += a.ssq_in[(size_t)q * a.B + b];
+        rs = 1.0f / sqrtf(ss / (float)a.ssq_K + a.eps);
+      }
+      s_rstd[b] = rs;
+      if (a.rstd_out && blockIdx.x == 0) a.rstd_out[b] = rs;
+    }
   }
   __syncwarp();
 
   // ---- epilogue ----------------------------------------------------------------------
   const bool done = mbar_wait(smem_u32(&bars[2 * C::kStages]), 0);
   if (!done) *abort_flag = 1;
+  pdl_trigger();   // main loop over: the next kernel may start launching
   __syncthreads();
   const bool ok = !*abort_flag && nkb > 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -294,6 +314,11 @@ __global__ void __launch_bounds__(128, 2)
   // ---- final epilogue, single split: straight from the accumulator registers ------------
   if (a.splits == 1) {
     if (!ok) return;
+    if (norm_in) {
+#pragma unroll
+      for (int b = 0; b < N / 2; ++b)
+        if (b < B) acc[b] *= s_rstd[b];
+    }
     if (a.epi == EPI_SILU) {
       float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
       if (r >= 64) {
@@ -313,10 +338,34 @@ __global__ void __launch_bounds__(128, 2)
       }
       return;
     }
-    if (!row_ok) return;
+    if (!norm_out) {
+      if (!row_ok) return;
 #pragma unroll
-    for (int b = 0; b < N / 2; ++b)
-      if (b < B) epi_store(a, b, m, acc[b]);
+      for (int b = 0; b < N / 2; ++b)
+        if (b < B) epi_store(a, b, m, acc[b]);
+      return;
+    }
+    // producer of a fused RMSNorm: y, the next operand and the tile's sums of y^2
+    constexpr int PB1 = N / 2 + 1;
+    float* sq = reinterpret_cast<float*>(smem);      // [128][PB1] y^2, stages idle now
+#pragma unroll
+    for (int b = 0; b < N / 2; ++b) {
+      if (b < B) {
+        float y = 0.f;
+        if (row_ok) {
+          y = acc[b] + epi_extra(a, b, m);
+          a.Y[(size_t)b * a.ldy + m] = y;
+          op_store(a.norm_op, a.M, Bp, b, m, a.norm_alpha[m] * y);
+        }
+        sq[r * PB1 + b] = y * y;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < B) {
+      float ss = 0.f;
+      for (int rr = 0; rr < 128; ++rr) ss += sq[rr * PB1 + threadIdx.x];
+      a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
+    }
     return;
   }
 
@@ -325,11 +374,14 @@ __global__ void __launch_bounds__(128, 2)
   // barrier, CTA `sp` reduces a slice of the tile's rows by reading the S partials
   // through distributed shared memory in split order 0..S-1, and applies the epilogue.
   // Every CTA passes both cluster barriers, also after a timeout.
-  constexpr int PB = N / 2 + 1;                     // padded row stride of a partial
+  // The partial is parked slot-major, [slot][row] with a padded row count, so that the
+  // reducing threads (rows fastest) read contiguous runs of peer memory and write
+  // contiguous rows of y and of the next operand.
+  constexpr int PR = 129;
   float* mine = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int b = 0; b < N / 2; ++b)
-    if (b < B) mine[r * PB + b] = ok ? acc[b] : 0.f;
+    if (b < B) mine[b * PR + r] = ok ? acc[b] : 0.f;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int S = a.splits;
@@ -339,19 +391,21 @@ __global__ void __launch_bounds__(128, 2)
   if (a.epi == EPI_SILU) {
     const int p0 = (sp * 64) / S, p1 = ((sp + 1) * 64) / S;
     const int n = (p1 - p0) * B;
+    const int prs = p1 - p0;
     for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const int p = p0 + e / B, b = e % B;
+      const int p = p0 + e % prs, b = e / prs;
       float gv[kMaxSplits], uv[kMaxSplits];
 #pragma unroll
       for (int q = 0; q < kMaxSplits; ++q)
         if (q < S) {
-          gv[q] = peer[q][p * PB + b];
-          uv[q] = peer[q][(p + 64) * PB + b];
+          gv[q] = peer[q][b * PR + p];
+          uv[q] = peer[q][b * PR + p + 64];
         }
       float g = 0.f, u = 0.f;
 #pragma unroll
       for (int q = 0; q < kMaxSplits; ++q)
         if (q < S) { g += gv[q]; u += uv[q]; }
+      if (norm_in) { g *= s_rstd[b]; u *= s_rstd[b]; }
       const int mm = mt * 64 + p;
       if (mm < a.pair_rows) op_store(a.op_out, a.ld_op, a.Bp_out, b, mm, g / (1.0f + expf(-g)) * u);
     }
@@ -361,15 +415,17 @@ __global__ void __launch_bounds__(128, 2)
     const int r0 = (sp * 128) / S, r1 = ((sp + 1) * 128) / S;
     const int n = (r1 - r0) * B;
     constexpr int CH = 8;
+    float* sq = mine + (N / 2) * PR;  // [slot][row - r0] y^2 of this slice (fused RMSNorm)
+    const int rows = r1 - r0;
     for (int e0 = threadIdx.x; e0 < n; e0 += CH * (int)blockDim.x) {
       int off[CH], mrow[CH], bcol[CH];
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
+      for (int i = 0; i < CH; ++i) {   // rows fastest across threads: coalesced y / operand
         const int e = e0 + i * (int)blockDim.x;
-        const int rr = r0 + e / B;
-        bcol[i] = e % B;
+        const int rr = r0 + e % rows;
+        bcol[i] = e / rows;
         mrow[i] = (e < n) ? mt * 128 + rr : a.M;     // a.M marks "no element"
-        off[i] = rr * PB + bcol[i];
+        off[i] = bcol[i] * PR + rr;
       }
       float ex[CH];
 #pragma unroll
@@ -383,13 +439,30 @@ __global__ void __launch_bounds__(128, 2)
           if (q < S && mrow[i] < a.M) pv[i][q] = peer[q][off[i]];
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
+        const int e = e0 + i * (int)blockDim.x;
         if (mrow[i] < a.M) {
           float v = 0.f;
 #pragma unroll
           for (int q = 0; q < kMaxSplits; ++q)
             if (q < S) v += pv[i][q];
-          a.Y[(size_t)bcol[i] * a.ldy + mrow[i]] = v + ex[i];
+          if (norm_in) v *= s_rstd[bcol[i]];
+          const float y = v + ex[i];
+          a.Y[(size_t)bcol[i] * a.ldy + mrow[i]] = y;
+          if (norm_out) {
+            op_store(a.norm_op, a.M, Bp, bcol[i], mrow[i], a.norm_alpha[mrow[i]] * y);
+            sq[off[i] - r0] = y * y;
+          }
+        } else if (norm_out && e < n) {
+          sq[off[i] - r0] = 0.f;     // rows past the matrix add nothing
         }
+      }
+    }
+    if (norm_out) {   // this slice's sums of y^2, in row order
+      __syncthreads();
+      if (threadIdx.x < B) {
+        float ss = 0.f;
+        for (int rr = 0; rr < r1 - r0; ++rr) ss += sq[threadIdx.x * PR + rr];
+        a.ssq_out[((size_t)mt * S + sp) * B + threadIdx.x] = ss;
       }
     }
   }

@@ -202,6 +202,8 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.op_dd = cv.take<uint16_t>(R * D.dd);
     b.op_do = cv.take<uint16_t>(R * D.dd);
     b.op_fd = cv.take<uint16_t>(R * D.Fd);
+    b.ssq = cv.take<float>((size_t)kMaxUnits * Bs);
+    b.rstd_z = cv.take<float>(Bs);
     if (grp) {
       grp[g].slot0 = slot0;
       grp[g].D = D;
@@ -302,9 +304,32 @@ bool plan_all(Group* e, int nsm) {
 }
 
 // One tensor-core contraction launch: matrix `row0` rows into its stacked tensor.
+// Fused RMSNorm wiring of one contraction launch: what it consumes (partials of the
+// producer before it, or a stored 1/rms) and what it produces for the next one.
+struct NormIO {
+  const float* ssq_in = nullptr;
+  int nparts = 0;
+  int K = 0;
+  const float* rstd_in = nullptr;
+  float* rstd_out = nullptr;
+  const float* alpha_out = nullptr;   // alpha of the next norm (producer)
+  uint16_t* op_next = nullptr;
+  float* ssq_out = nullptr;
+};
+
 cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, int epi, float* Y,
-                      int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s) {
+                      int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s,
+                      const NormIO& nio = NormIO()) {
   UmmaArgs a{};
+  a.ssq_in = nio.ssq_in;
+  a.ssq_nparts = nio.nparts;
+  a.ssq_K = nio.K;
+  a.eps = D.eps;
+  a.rstd_in = nio.rstd_in;
+  a.rstd_out = nio.rstd_out;
+  a.norm_alpha = nio.alpha_out;
+  a.norm_op = nio.op_next;
+  a.ssq_out = nio.ssq_out;
   a.M = g.M;
   a.pair_rows = g.pair;
   a.row0 = row0;
@@ -330,68 +355,111 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
     if (prof) PP_TRY(prof->mark((k), s));       \
   } while (0)
 
-// The tick with every weight contraction on the tensor cores.
+// The tick with every weight contraction on the tensor cores.  RMSNorms are fused: each
+// residual-producing contraction writes the next contraction's operand (alpha * y, split
+// bf16) and per-slice sums of y^2; the consuming contraction scales by 1/rms.
 cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s, Prof* prof) {
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
+  const int p_o = mm[MM_O].m_tiles * mm[MM_O].splits;
+  const int p_down = mm[MM_DOWN].m_tiles * mm[MM_DOWN].splits;
+  const int p_din = mm[MM_DIN].m_tiles * mm[MM_DIN].splits;
+  const int p_do = mm[MM_DO].m_tiles * mm[MM_DO].splits;
+  const int p_ddown = mm[MM_DDOWN].m_tiles * mm[MM_DDOWN].splits;
   MARK(PP_K_BEGIN);
-  PP_TRY(launch_begin(D, b, s));
+  PP_TRY(launch_begin(D, b, b.attn_alpha, b.op_d, b.ssq, s));
   for (int l = 0; l < D.L; ++l) {
-    MARK(PP_K_NORM);
-    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, nullptr, 0, b.op_d, s));
+    NormIO qn;
+    qn.ssq_in = b.ssq;
+    qn.nparts = (l == 0) ? 1 : p_down;
+    qn.K = D.d;
     MARK(PP_K_QKV);
-    PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_STORE, b.qkv, 3 * D.d, nullptr, nullptr, 0, s));
+    PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_STORE, b.qkv, 3 * D.d, nullptr, nullptr, 0, s, qn));
     MARK(PP_K_ROPE_RING);
     PP_TRY(launch_rope_ring(D, b, l, s));
     MARK(PP_K_ATTN);
     PP_TRY(launch_attn(D, b, l, true, s));
+    NormIO on;
+    on.alpha_out = b.mlp_alpha + (size_t)l * D.d;
+    on.op_next = b.op_d;
+    on.ssq_out = b.ssq;
     MARK(PP_K_OPROJ);
-    PP_TRY(mm_launch(D, b, mm[MM_O], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s));
-    MARK(PP_K_NORM);
-    PP_TRY(launch_rmsnorm(D, b.x, D.d, b.mlp_alpha + (size_t)l * D.d, D.d, nullptr, 0, b.op_d, s));
+    PP_TRY(mm_launch(D, b, mm[MM_O], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s, on));
+    NormIO gn;
+    gn.ssq_in = b.ssq;
+    gn.nparts = p_o;
+    gn.K = D.d;
     MARK(PP_K_GATEUP);
-    PP_TRY(mm_launch(D, b, mm[MM_GU], l * 2 * D.F, EPI_SILU, nullptr, 0, nullptr, b.op_f, D.F, s));
+    PP_TRY(mm_launch(D, b, mm[MM_GU], l * 2 * D.F, EPI_SILU, nullptr, 0, nullptr, b.op_f, D.F, s, gn));
+    NormIO dn;
+    const bool last = (l + 1 == D.L);
+    dn.alpha_out = last ? b.out_alpha : b.attn_alpha + (size_t)(l + 1) * D.d;
+    dn.op_next = last ? b.op_z : b.op_d;
+    dn.ssq_out = b.ssq;
     MARK(PP_K_DOWN);
-    PP_TRY(mm_launch(D, b, mm[MM_DOWN], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s));
+    PP_TRY(mm_launch(D, b, mm[MM_DOWN], l * D.d, EPI_ADD, b.x, D.d, nullptr, nullptr, 0, s, dn));
   }
-  MARK(PP_K_TEXT_HEAD);
-  PP_TRY(launch_rmsnorm(D, b.x, D.d, b.out_alpha, D.d, nullptr, 0, b.op_z, s));
-  MARK(PP_K_TEXT_HEAD);
-  PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s));
+  {
+    NormIO tn;
+    tn.ssq_in = b.ssq;
+    tn.nparts = p_down;
+    tn.K = D.d;
+    tn.rstd_out = b.rstd_z;     // kept for the 16 depformer input projections
+    MARK(PP_K_TEXT_HEAD);
+    PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s, tn));
+  }
   MARK(PP_K_TEXT_HEAD);
   PP_TRY(launch_text_argmax(D, b, s));
   g_launch_priority = dep_priority;   // the latency-bound depformer goes first
   for (int k = 0; k < D.nq; ++k) {
     const uint16_t* emb =
         (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
+    NormIO in;
+    in.rstd_in = b.rstd_z;
+    in.alpha_out = b.dep_attn_alpha;
+    in.op_next = b.op_dd;
+    in.ssq_out = b.ssq;
     MARK(PP_K_DEP_INPROJ);
-    PP_TRY(mm_launch(D, b, mm[MM_DIN], k * D.dd, EPI_EMB, b.y, D.dd, emb, nullptr, 0, s));
+    PP_TRY(mm_launch(D, b, mm[MM_DIN], k * D.dd, EPI_EMB, b.y, D.dd, emb, nullptr, 0, s, in));
     for (int j = 0; j < D.Ld; ++j) {
-      MARK(PP_K_DEP_NORM);
-      PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_attn_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
-                            b.op_dd, s));
+      NormIO qn;
+      qn.ssq_in = b.ssq;
+      qn.nparts = (j == 0) ? p_din : p_ddown;
+      qn.K = D.dd;
       MARK(PP_K_DEP_QKV);
       PP_TRY(mm_launch(D, b, mm[MM_DQKV], j * 3 * D.dd, EPI_STORE, b.dqkv, 3 * D.dd, nullptr,
-                       nullptr, 0, s));
+                       nullptr, 0, s, qn));
       MARK(PP_K_DEP_ATTN);
       PP_TRY(launch_dep_attn(D, b, k, j, true, s));
+      NormIO on;
+      on.alpha_out = b.dep_mlp_alpha + (size_t)j * D.dd;
+      on.op_next = b.op_dd;
+      on.ssq_out = b.ssq;
       MARK(PP_K_DEP_OPROJ);
-      PP_TRY(mm_launch(D, b, mm[MM_DO], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
-      MARK(PP_K_DEP_NORM);
-      PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_mlp_alpha + (size_t)j * D.dd, D.dd, nullptr, 0,
-                            b.op_dd, s));
+      PP_TRY(mm_launch(D, b, mm[MM_DO], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s, on));
+      NormIO gn;
+      gn.ssq_in = b.ssq;
+      gn.nparts = p_do;
+      gn.K = D.dd;
       MARK(PP_K_DEP_GATEUP);
       PP_TRY(mm_launch(D, b, mm[MM_DGU], j * 2 * D.Fd, EPI_SILU, nullptr, 0, nullptr, b.op_fd,
-                       D.Fd, s));
+                       D.Fd, s, gn));
+      NormIO dn;
+      const bool last = (j + 1 == D.Ld);
+      dn.alpha_out = last ? b.dep_out_alpha : b.dep_attn_alpha + (size_t)(j + 1) * D.dd;
+      dn.op_next = b.op_dd;
+      dn.ssq_out = b.ssq;
       MARK(PP_K_DEP_DOWN);
-      PP_TRY(mm_launch(D, b, mm[MM_DDOWN], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s));
+      PP_TRY(mm_launch(D, b, mm[MM_DDOWN], j * D.dd, EPI_ADD, b.y, D.dd, nullptr, nullptr, 0, s, dn));
     }
-    MARK(PP_K_DEP_NORM);
-    PP_TRY(launch_rmsnorm(D, b.y, D.dd, b.dep_out_alpha, D.dd, nullptr, 0, b.op_dd, s));
+    NormIO hn;
+    hn.ssq_in = b.ssq;
+    hn.nparts = p_ddown;
+    hn.K = D.dd;
     MARK(PP_K_DEP_HEAD);
     PP_TRY(mm_launch(D, b, mm[MM_DHEAD], k * D.Va, EPI_STORE, b.logits + D.Vt + (size_t)k * D.Va,
-                     D.logits_ld, nullptr, nullptr, 0, s));
+                     D.logits_ld, nullptr, nullptr, 0, s, hn));
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
   }
@@ -405,7 +473,7 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
 // recorded before every launch (and once at the end).
 cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Prof* prof) {
   MARK(PP_K_BEGIN);
-  PP_TRY(launch_begin(D, b, s));
+  PP_TRY(launch_begin(D, b, nullptr, nullptr, nullptr, s));
   for (int l = 0; l < D.L; ++l) {
     MARK(PP_K_NORM);
     PP_TRY(launch_rmsnorm(D, b.x, D.d, b.attn_alpha + (size_t)l * D.d, D.d, b.xn, D.d, nullptr, s));

@@ -86,6 +86,8 @@ struct Buffers {
   uint16_t* op_dd;         // K = dd  (normalised depformer stream)
   uint16_t* op_do;         // K = dd  (depformer attention output)
   uint16_t* op_fd;         // K = Fd  (depformer gated hidden)
+  float* ssq;              // fused-RMSNorm partial sums of squares [kMaxUnits][B]
+  float* rstd_z;           // [B] 1/rms of the temporal output (text head and depformer input)
 };
 
 constexpr int kMaxUnits = 4096;      // cap on (M-tile x K-split) units of one contraction
@@ -93,12 +95,16 @@ constexpr int kMaxSplits = 8;        // K-splits of one tile form one (portable)
 constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction
 
 // ---- programmatic dependent launch ------------------------------------------------------
-// Every kernel of the tick is launched with programmatic stream serialization: it may
-// start while its predecessor drains, waits (griddepcontrol.wait) for the predecessor's
-// completion and memory flush before touching any data, and lets its own successor
-// launch right away.
+// With PP_FLAG_PDL the tick's kernels are launched with programmatic stream
+// serialization: a kernel may start while its predecessor drains, and waits
+// (griddepcontrol.wait) for the predecessor's completion and memory flush before it
+// touches any data.  The long kernels let their successor launch once their main work
+// is done (pdl_trigger); the others trigger implicitly when they exit.  Without the
+// flag both instructions are no-ops.
 __device__ __forceinline__ void pdl_wait_and_trigger() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -138,7 +144,9 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 }
 
 // ---- launchers (stream-ordered; return cudaGetLastError) ----------------------------
-cudaError_t launch_begin(const Dims& D, const Buffers& b, cudaStream_t s);
+// op (may be null): also write the layer-0 operand hi/lo(alpha * x) and the sum of x^2
+cudaError_t launch_begin(const Dims& D, const Buffers& b, const float* alpha, uint16_t* op,
+                         float* ssq, cudaStream_t s);
 // out (fp32, may be null) and/or op (bf16 hi/lo operand [2*Bp][K], may be null)
 cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
                            float* out, int ldo, uint16_t* op, cudaStream_t s);
@@ -173,6 +181,21 @@ struct UmmaArgs {
   int ld_op;
   int Bp_out;
   uint32_t* status;
+  // Fused RMSNorm, producer side (EPI_ADD / EPI_EMB): besides y, write the next
+  // contraction's operand hi/lo(norm_alpha * y) [2*Bp][M] and the partial sums of y^2 of
+  // this launch's (tile, split) row slices, ssq_out[(tile * splits + split) * B + b].
+  const float* norm_alpha;
+  uint16_t* norm_op;
+  float* ssq_out;
+  // Fused RMSNorm, consumer side: scale the contraction by 1/rms of the input, from the
+  // producer's partials (ssq_in, ssq_nparts slices, width ssq_K) or precomputed
+  // (rstd_in); block 0 also stores the values in rstd_out when it is given.
+  const float* ssq_in;
+  int ssq_nparts;
+  int ssq_K;
+  float eps;
+  const float* rstd_in;
+  float* rstd_out;
 };
 cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                         cudaStream_t s);

@@ -14,6 +14,7 @@ pytestmark = pytest.mark.gpu
 FULL = synth.FULL
 SEED = 1
 TICKS = int(os.environ.get("PP_FULL_TICKS", "40"))   # 250 runs the whole prefill workload
+FLAGS = int(os.environ.get("PP_FULL_FLAGS", "0"))    # engine flags (1: CUDA-core contractions)
 
 
 @pytest.fixture(scope="module")
@@ -41,7 +42,7 @@ def test_full_b1_prefill_parity(full_weights):
     """Voice prefill, silence, persona text: teacher-forced, every tick."""
     w_host, w_dev = full_weights
     user, fm, fo = schedules.prefill_session(FULL, SEED, T=TICKS)
-    st = run_parity(FULL, 1, w_host, w_dev, [Placement(0, 0, Script(user, fm, fo))])
+    st = run_parity(FULL, 1, w_host, w_dev, [Placement(0, 0, Script(user, fm, fo))], flags=FLAGS)
     print("full b1", st)
     assert st["status"] == 0 and st["ticks"] == TICKS
 
@@ -71,6 +72,6 @@ def test_full_b64_full_ring_sampled(full_weights):
 
     pl = [Placement(s, 0, greedy_script(FULL, 2, 50 + s), import_pos=W, check=s in checked)
           for s in range(64)]
-    st = run_parity(FULL, 64, w_host, w_dev, pl, oracle_sessions=ora, setup=setup)
+    st = run_parity(FULL, 64, w_host, w_dev, pl, oracle_sessions=ora, setup=setup, flags=FLAGS)
     print("full b64", st)
     assert st["status"] == 0
