@@ -57,7 +57,7 @@ class pp_config(ctypes.Structure):
         ("eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", ctypes.c_int32)]
 
 PP_FLAG_CUDA_CORE_GEMM = 0x1
-PP_FLAG_PDL = 0x2
+PP_FLAG_NO_PDL = 0x2
 PP_FLAG_TWO_GROUPS = 0x4
 
 

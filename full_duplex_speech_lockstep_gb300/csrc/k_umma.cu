@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(128, 2)
   const bool norm_in = a.ssq_in != nullptr || a.rstd_in != nullptr;
   const bool norm_out = a.norm_alpha != nullptr;
 
-  pdl_wait_and_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.splits, sp = blockIdx.x % a.splits;
   const int kb0 = (int)(((long long)sp * a.kblocks) / a.splits);
@@ -210,6 +209,19 @@ __global__ void __launch_bounds__(128, 2)
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer ------------------------------------------------------------------
+    // The weights do not depend on the previous kernel: the first stages' weight tiles
+    // are requested before waiting for it (programmatic dependent launch), the
+    // activation tiles after.
+    const int pre = nkb < C::kStages ? nkb : C::kStages;
+    for (int i = 0; i < pre; ++i) {
+      uint8_t* sa = smem + i * C::kStageBytes;
+      const uint32_t full = smem_u32(&bars[i]);
+      mbar_expect_tx(full, C::kStageBytes);
+      const int kx = (kb0 + i) * kBK;
+      tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
+      tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+    }
+    pdl_wait_and_trigger();
     int issued = 0;
     for (int i = 0; i < nkb; ++i) {
       const int s = i % C::kStages;
@@ -222,15 +234,19 @@ __global__ void __launch_bounds__(128, 2)
       uint8_t* sa = smem + s * C::kStageBytes;
       uint8_t* sb = sa + C::kABytes;
       const uint32_t full = smem_u32(&bars[s]);
-      mbar_expect_tx(full, C::kStageBytes);
       const int kx = (kb0 + i) * kBK;
-      tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
-      tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+      if (i >= pre) {
+        mbar_expect_tx(full, C::kStageBytes);
+        tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
+        tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+      }
       tma_load_2d(smem_u32(sb), &mapB, kx, 0, full);
       ++issued;
     }
-    if (*abort_flag) {  // drain this CTA's copies still in flight (bounded)
-      for (int i = 0; i < issued; ++i) mbar_wait(smem_u32(&bars[i % C::kStages]), (i / C::kStages) & 1);
+    if (*abort_flag) {  // drain this CTA's copies still in flight (bounded waits)
+      const int inflight = issued > pre ? issued : pre;
+      for (int i = 0; i < inflight; ++i)
+        mbar_wait(smem_u32(&bars[i % C::kStages]), (i / C::kStages) & 1);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer --------------------------------------------------------------------
@@ -252,6 +268,7 @@ __global__ void __launch_bounds__(128, 2)
     }
     umma_commit(smem_u32(&bars[2 * C::kStages]));
   } else if (warp >= 2 && norm_in) {
+    pdl_wait_and_trigger();
     // fused RMSNorm of the input: 1/rms of every slot, summed from the producer's
     // partials in slice order while the main loop runs
     for (int b = threadIdx.x - 64; b < a.B; b += 64) {
@@ -268,6 +285,7 @@ __global__ void __launch_bounds__(128, 2)
       if (a.rstd_out && blockIdx.x == 0) a.rstd_out[b] = rs;
     }
   }
+  if (!(warp == 0 && lane == 0)) pdl_wait_and_trigger();   // (a no-op when done twice)
   __syncwarp();
 
   // ---- epilogue ----------------------------------------------------------------------

@@ -692,7 +692,7 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   e->open.assign(e->B, 0);
 
   e->tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
-  g_use_pdl = (c->flags & PP_FLAG_PDL) != 0;   // read while this engine's graphs are captured
+  g_use_pdl = !(c->flags & PP_FLAG_NO_PDL);   // read while this engine's graphs are captured
   cudaError_t err = cudaSuccess;
   {  // zero the per-slot state (positions, liveness, control, status)
     const Buffers& sh = e->shared;

@@ -95,12 +95,12 @@ constexpr int kMaxSplits = 8;        // K-splits of one tile form one (portable)
 constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction
 
 // ---- programmatic dependent launch ------------------------------------------------------
-// With PP_FLAG_PDL the tick's kernels are launched with programmatic stream
-// serialization: a kernel may start while its predecessor drains, and waits
+// The tick's kernels are launched with programmatic stream serialization (unless
+// PP_FLAG_NO_PDL): a kernel may start while its predecessor drains, and waits
 // (griddepcontrol.wait) for the predecessor's completion and memory flush before it
-// touches any data.  The long kernels let their successor launch once their main work
-// is done (pdl_trigger); the others trigger implicitly when they exit.  Without the
-// flag both instructions are no-ops.
+// touches any data the predecessor may write.  The long kernels let their successor
+// launch once their main work is done (pdl_trigger); the others trigger implicitly when
+// they exit.  Without the launch attribute both instructions are no-ops.
 __device__ __forceinline__ void pdl_wait_and_trigger() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -78,10 +78,11 @@ typedef struct {
  * tcgen05 tensor-core path (split-bf16 activations).  The two paths round
  * differently, so a session's bits are reproducible within one path only. */
 #define PP_FLAG_CUDA_CORE_GEMM 0x1
-/* Launch the tick's kernels with programmatic dependent launch (each kernel may start
- * while its predecessor drains and waits for it in-kernel).  Off by default: on GB300
- * the tick measured faster without it. */
-#define PP_FLAG_PDL 0x2
+/* Launch the tick's kernels without programmatic dependent launch.  By default each
+ * kernel may start while its predecessor drains: a contraction allocates its tensor
+ * memory and streams its first weight tiles (weights never depend on the previous
+ * kernel), then waits for the predecessor before it reads any activation. */
+#define PP_FLAG_NO_PDL 0x2
 /* Split an engine of 16 or more slots into two groups that run as parallel branches of
  * the tick graph, so one group's latency-bound depformer can overlap the other's
  * bandwidth-bound attention (weights are then streamed once per group).  Off by

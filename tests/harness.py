@@ -13,7 +13,12 @@ import dataclasses
 
 import numpy as np
 
+import os
+
 ROWS = 17
+# extra engine flags for every engine the GPU tests create (e.g. 2 = PP_FLAG_PDL), so the
+# same suite can check the tick under another launch mode
+EXTRA_FLAGS = int(os.environ.get("PP_TEST_FLAGS", "0"))
 LOGIT_TOL = 2e-2        # max |gpu - oracle| <= LOGIT_TOL * std(oracle logits)
 TOKEN_MARGIN = 1e-2     # tokens must agree where the oracle's top-2 margin exceeds this
 
@@ -73,7 +78,7 @@ def run_parity(shape, B, w_host, w_dev, placements, check_logits=True, report=No
     import oracle
 
     orc = oracle.Oracle(shape, w_host)
-    eng = pp.Engine(shape, B, w_dev, flags=flags)
+    eng = pp.Engine(shape, B, w_dev, flags=flags | EXTRA_FLAGS)
     if setup is not None:
         setup(eng)
     T_end = max(p.start + p.script.T for p in placements)

@@ -8,7 +8,7 @@ import pytest
 
 import synth
 from synth import schedules
-from harness import ROWS, device_weights, initial_column
+from harness import EXTRA_FLAGS, ROWS, device_weights, initial_column
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +61,12 @@ def pp_flags_two_groups():
 
 def _check_isolation(shape, B, sessions, T_end, w_dev, flags=0):
     import full_duplex_speech_lockstep_gb300 as pp
-    eng = pp.Engine(shape, B, w_dev, flags=flags)
+    eng = pp.Engine(shape, B, w_dev, flags=flags | EXTRA_FLAGS)
     batched = _run(eng, B, shape, sessions, T_end)
     assert eng.status() == 0
     eng.close_engine()
     for i, (slot, start, user, fm, fo) in enumerate(sessions):
-        e1 = pp.Engine(shape, 1, w_dev)
+        e1 = pp.Engine(shape, 1, w_dev, flags=EXTRA_FLAGS)
         alone = _run(e1, 1, shape, [(0, 0, user, fm, fo)], user.shape[0])
         e1.close_engine()
         bc, bl = np.array(batched[i][0]), np.array(batched[i][1])
@@ -97,7 +97,7 @@ def test_grouping_does_not_change_bits():
         sessions.append((i, i % 3, user, fm, fo))
     outs = []
     for flags in [0, pp.PP_FLAG_TWO_GROUPS]:
-        e = pp.Engine(s, 20, w, flags=flags)
+        e = pp.Engine(s, 20, w, flags=flags | EXTRA_FLAGS)
         outs.append(_run(e, 20, s, sessions, 18))
         e.close_engine()
     for i in range(len(sessions)):
