@@ -16,7 +16,7 @@ import numpy as np
 import os
 
 ROWS = 17
-# extra engine flags for every engine the GPU tests create (e.g. 2 = PP_FLAG_PDL), so the
+# extra engine flags for every engine the GPU tests create (e.g. 2 = PP_FLAG_NO_PDL), so the
 # same suite can check the tick under another launch mode
 EXTRA_FLAGS = int(os.environ.get("PP_TEST_FLAGS", "0"))
 LOGIT_TOL = 2e-2        # max |gpu - oracle| <= LOGIT_TOL * std(oracle logits)
