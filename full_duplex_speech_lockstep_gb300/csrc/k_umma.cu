@@ -277,8 +277,14 @@ __global__ void __launch_bounds__(128, 2)
         rs = a.rstd_in[b];
       } else {
         float ss = 0.f;
-#pragma unroll 8
-        for (int q = 0; q < a.ssq_nparts; ++q) ss += a.ssq_in[(size_t)q * a.B + b];
+        for (int q0 = 0; q0 < a.ssq_nparts; q0 += 16) {   // 16 loads in flight, added in order
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            v[i] = (q0 + i < a.ssq_nparts) ? a.ssq_in[(size_t)(q0 + i) * a.B + b] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ss += v[i];
+        }
         rs = 1.0f / sqrtf(ss / (float)a.ssq_K + a.eps);
       }
       s_rstd[b] = rs;
@@ -475,16 +481,25 @@ __global__ void __launch_bounds__(128, 2)
         }
       }
     }
-    if (norm_out) {   // this slice's sums of y^2, in row order
+    if (norm_out) {   // this slice's sums of y^2, in row order, parked for CTA 0 of the tile
       __syncthreads();
       if (threadIdx.x < B) {
         float ss = 0.f;
         for (int rr = 0; rr < r1 - r0; ++rr) ss += sq[threadIdx.x * PR + rr];
-        a.ssq_out[((size_t)mt * S + sp) * B + threadIdx.x] = ss;
+        s_rstd[threadIdx.x] = ss;      // (its 1/rms values, if any, are no longer needed)
       }
     }
   }
   cluster.sync();   // peers may still be reading this CTA's partial until here
+  if (norm_out && a.epi != EPI_SILU) {
+    // CTA 0 of the tile adds the slices' sums in split order: one partial per tile
+    if (sp == 0 && threadIdx.x < B) {
+      float ss = 0.f;
+      for (int q = 0; q < S; ++q) ss += cluster.map_shared_rank(s_rstd, q)[threadIdx.x];
+      a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
+    }
+    cluster.sync();   // peers stay until CTA 0 has read their sums
+  }
   if (!ok && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
 }
 

@@ -362,11 +362,12 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
-  const int p_o = mm[MM_O].m_tiles * mm[MM_O].splits;
-  const int p_down = mm[MM_DOWN].m_tiles * mm[MM_DOWN].splits;
-  const int p_din = mm[MM_DIN].m_tiles * mm[MM_DIN].splits;
-  const int p_do = mm[MM_DO].m_tiles * mm[MM_DO].splits;
-  const int p_ddown = mm[MM_DDOWN].m_tiles * mm[MM_DDOWN].splits;
+  // fused-norm partials: one per M-tile of the producing contraction
+  const int p_o = mm[MM_O].m_tiles;
+  const int p_down = mm[MM_DOWN].m_tiles;
+  const int p_din = mm[MM_DIN].m_tiles;
+  const int p_do = mm[MM_DO].m_tiles;
+  const int p_ddown = mm[MM_DDOWN].m_tiles;
   MARK(PP_K_BEGIN);
   PP_TRY(launch_begin(D, b, b.attn_alpha, b.op_d, b.ssq, s));
   for (int l = 0; l < D.L; ++l) {

@@ -182,8 +182,8 @@ struct UmmaArgs {
   int Bp_out;
   uint32_t* status;
   // Fused RMSNorm, producer side (EPI_ADD / EPI_EMB): besides y, write the next
-  // contraction's operand hi/lo(norm_alpha * y) [2*Bp][M] and the partial sums of y^2 of
-  // this launch's (tile, split) row slices, ssq_out[(tile * splits + split) * B + b].
+  // contraction's operand hi/lo(norm_alpha * y) [2*Bp][M] and the sums of y^2 over each
+  // M-tile's rows, ssq_out[tile * B + b] (the splits of a tile are added in order).
   const float* norm_alpha;
   uint16_t* norm_op;
   float* ssq_out;
