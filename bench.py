@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="full", choices=["tiny", "small", "full"])
     ap.add_argument("--engine-flags", type=int, default=0, help="pp_config.flags (PP_FLAG_*)")
+    ap.add_argument("--skip-user-steps-steps", type=int, default=50,
+                    help="ticks of the secondary measurement with PP_FLAG_SKIP_USER_STEPS "
+                         "(0 = skip it)")
     ap.add_argument("--layers", type=int, default=0,
                     help="temporal layers (0 = the shape's own); fewer layers give a small "
                          "case with full-size kernels for profiling")
@@ -386,6 +389,21 @@ def main():
     del eng
     torch.cuda.empty_cache()
 
+    # -- the same workload with depformer steps 8..15 elided (user rows, same columns) -----
+    skip = None
+    if a.skip_user_steps_steps > 0:
+        e2 = pp.Engine(shape, B, w_dev, flags=a.engine_flags | pp.PP_FLAG_SKIP_USER_STEPS)
+        fill_rings(e2, shape, B, pos)
+        ms2, per2 = time_ticks(e2, B, shape, a.skip_user_steps_steps, max(3, a.warmup // 4), 800)
+        ms2 = max_over_ranks(ws, ms2)
+        skip = {"value": sum_over_ranks(ws, B * a.skip_user_steps_steps) / (ms2 / 1000.0),
+                "unit": UNIT, "ms_per_step": ms2 / a.skip_user_steps_steps,
+                "p50_tick_ms": float(np.percentile(per2, 50)),
+                "note": "PP_FLAG_SKIP_USER_STEPS: identical columns; user-row logits not computed"}
+        e2.close_engine()
+        del e2
+        torch.cuda.empty_cache()
+
     # -- B=1 latency line (full shape, fresh session) ---------------------------------------
     b1 = None
     if a.b1_steps > 0:
@@ -424,6 +442,7 @@ def main():
             "roofline": roofline,
             "kernels_profile": prof,
             "b1": b1,
+            "skip_user_steps": skip,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": cpu,

@@ -59,6 +59,7 @@ class pp_config(ctypes.Structure):
 PP_FLAG_CUDA_CORE_GEMM = 0x1
 PP_FLAG_NO_PDL = 0x2
 PP_FLAG_TWO_GROUPS = 0x4
+PP_FLAG_SKIP_USER_STEPS = 0x8
 
 
 class pp_weights(ctypes.Structure):

@@ -372,6 +372,26 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
   return cudaGetLastError();
 }
 
+// Rows 9..16 straight from this frame's user codes (when depformer steps 8..15, whose
+// only other output is their logits, are not run).
+__global__ void k_user_rows(Dims D, Buffers b) {
+  pdl_wait_and_trigger();
+  const int s = blockIdx.x, r = threadIdx.x;
+  if (r >= PP_USER_ROWS) return;
+  const int row = PP_AGENT_ROWS + 1 + r;
+  if (!b.live[s]) {
+    b.out_col[s * kRows + row] = -1;
+    return;
+  }
+  int t = b.in_user[s * PP_USER_ROWS + r];
+  if (t < 0 || t > D.Va) { atomicOr(b.status, PP_S_INDEX); t = D.Va; }
+  b.out_col[s * kRows + row] = t;
+}
+
+cudaError_t launch_user_rows(const Dims& D, const Buffers& b, cudaStream_t s) {
+  return launch_k(k_user_rows, dim3(D.B), dim3(32), 0, s, 1, D, b);
+}
+
 // ---- end of tick -----------------------------------------------------------------------
 __global__ void k_finish(Dims D, Buffers b) {
   pdl_wait_and_trigger();

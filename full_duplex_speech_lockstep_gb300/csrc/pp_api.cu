@@ -112,6 +112,7 @@ Dims make_dims(const pp_config* c) {
   D.eps = c->eps; D.rope_base = c->rope_base;
   D.nc_max = (c->window + kAttnChunk - 1) / kAttnChunk;
   D.logits_ld = c->text_vocab + c->n_q * c->audio_card;
+  D.dep_steps = (c->flags & PP_FLAG_SKIP_USER_STEPS) ? c->n_q / 2 : c->n_q;
   return D;
 }
 
@@ -257,7 +258,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k, uint3
 // K-splits per M-tile: a function of the matrix shape and the device's SM count only,
 // never of the batch, so every engine size reduces in the same order.  Model: units run
 // in waves of two CTAs per SM; a unit costs its k-blocks plus a fixed overhead of about
-// three k-blocks (launch share, pipeline fill, epilogue).
+// five k-blocks (launch share, pipeline fill, epilogue; calibrated on GB300 by sweeping
+// the split counts of the full-size matrices at 64 slots).
 int choose_splits(int m_tiles, int kblocks, int nsm) {
   const int slots = 2 * nsm;
   int best = 1;
@@ -265,7 +267,7 @@ int choose_splits(int m_tiles, int kblocks, int nsm) {
   for (int sp = 1; sp <= kblocks && sp <= kMaxSplits && m_tiles * sp <= kMaxUnits; ++sp) {
     const int units = m_tiles * sp;
     const int waves = (units + slots - 1) / slots;
-    const double t = waves * ((double)((kblocks + sp - 1) / sp) + 3.0);
+    const double t = waves * ((double)((kblocks + sp - 1) / sp) + 5.0);
     if (t < best_t - 1e-9) { best_t = t; best = sp; }
   }
   return best;
@@ -413,7 +415,7 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   MARK(PP_K_TEXT_HEAD);
   PP_TRY(launch_text_argmax(D, b, s));
   g_launch_priority = dep_priority;   // the latency-bound depformer goes first
-  for (int k = 0; k < D.nq; ++k) {
+  for (int k = 0; k < D.dep_steps; ++k) {
     const uint16_t* emb =
         (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
     NormIO in;
@@ -463,6 +465,10 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
                      D.logits_ld, nullptr, nullptr, 0, s, hn));
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
+  }
+  if (D.dep_steps < D.nq) {
+    MARK(PP_K_DEP_HEAD);
+    PP_TRY(launch_user_rows(D, b, s));
   }
   MARK(PP_K_FINISH);
   PP_TRY(launch_finish(D, b, s));
@@ -516,7 +522,7 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
   }
   MARK(PP_K_TEXT_HEAD);
   PP_TRY(launch_text_argmax(D, b, s));
-  for (int k = 0; k < D.nq; ++k) {
+  for (int k = 0; k < D.dep_steps; ++k) {
     GemvArgs a{};
     a.W = b.dep_inproj + (size_t)k * D.dd * D.d; a.M = D.dd; a.K = D.d;
     a.X = b.z; a.ldx = D.d; a.Y = b.y; a.ldy = D.dd; a.epi = EPI_EMB;
@@ -562,6 +568,10 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
     PP_TRY(launch_gemv(D, a, s));
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
+  }
+  if (D.dep_steps < D.nq) {
+    MARK(PP_K_DEP_HEAD);
+    PP_TRY(launch_user_rows(D, b, s));
   }
   MARK(PP_K_FINISH);
   PP_TRY(launch_finish(D, b, s));

@@ -20,6 +20,7 @@ struct Dims {
   int nc_max;            // attention chunks per (slot, head) at a full ring
   int logits_ld;         // Vt + nq * Va
   int Bp;                // slots padded to a multiple of 8: operand rows are [hi: Bp][lo: Bp]
+  int dep_steps;         // depformer steps run (n_q, or n_q / 2 when the user rows are elided)
 };
 
 struct Buffers {
@@ -242,5 +243,6 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
                             cudaStream_t s);
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s);
 cudaError_t launch_finish(const Dims& D, const Buffers& b, cudaStream_t s);
+cudaError_t launch_user_rows(const Dims& D, const Buffers& b, cudaStream_t s);
 
 }  // namespace pp

@@ -89,6 +89,11 @@ typedef struct {
  * default: on GB300 the doubled weight traffic cost more than the overlap saved.
  * Grouping never changes a session's bits. */
 #define PP_FLAG_TWO_GROUPS 0x4
+/* Run depformer steps 0..7 only.  Steps 8..15 decide user rows 9..16, which always take
+ * the incoming user codes, so every column is unchanged; only their logits (the last 8
+ * codebook blocks of the logits output) are not computed and keep stale values.  Off by
+ * default: the default tick runs all 16 steps. */
+#define PP_FLAG_SKIP_USER_STEPS 0x8
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */

@@ -46,3 +46,36 @@ def test_paths_agree(B):
     a, b = outs
     scale = np.std(a)
     assert np.max(np.abs(a - b)) <= 1e-3 * scale
+
+
+def test_skip_user_steps_keeps_every_column():
+    """With PP_FLAG_SKIP_USER_STEPS the depformer runs steps 0..7 only: every column and
+    the text and agent-row logits are bit-identical to the 16-step tick."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    from harness import initial_column
+    s = synth.SMALL
+    w = device_weights(synth.make_weights_host(s, 23, alpha="random"))
+    B, T = 6, 12
+    Vt, Va = s.text_vocab, s.audio_card
+    ld = Vt + 16 * Va
+    user = synth.uniform_i32(T * B * 8, 4, 4, 0, Va).reshape(T, B, 8)
+    runs = []
+    for flags in [0, pp.PP_FLAG_SKIP_USER_STEPS]:
+        e = pp.Engine(s, B, w, flags=flags)
+        for b in range(B):
+            e.open(b)
+        prev = torch.from_numpy(np.tile(initial_column(s), (B, 1))).cuda()
+        lg = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+        cols, logits = [], []
+        for t in range(T):
+            col = e.step(prev, torch.from_numpy(user[t]).cuda(), logits=lg)
+            torch.cuda.synchronize()
+            cols.append(col.cpu().numpy().copy())
+            logits.append(lg.cpu().numpy()[:, :Vt + 8 * Va].copy())
+            prev = col.clone()
+        assert e.status() == 0
+        e.close_engine()
+        runs.append((np.array(cols), np.array(logits)))
+    assert np.array_equal(runs[0][0], runs[1][0])
+    assert np.array_equal(runs[0][1].view(np.uint32), runs[1][1].view(np.uint32))
