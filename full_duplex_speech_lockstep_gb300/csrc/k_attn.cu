@@ -5,26 +5,67 @@
 // one of the last W positions.  Softmax is invariant to the order of its keys, so the
 // kernel attends over ring indices directly.
 //
-// Grid (chunk, head, slot); a CTA of 8 warps covers 256 consecutive ring indices
-// (32 per warp).  Within a warp, a group of 4 lanes owns one key: each lane holds a
-// quarter of the head's 16-byte pieces of q and loads the matching pieces of K and V
-// with streaming 16-byte loads.  The warp partials are merged in warp order, then the
-// chunk partial (max, sum, unnormalised output) is written; the last CTA of a
-// (slot, head) to finish merges the chunks in chunk order.  Every reduction order is
-// fixed by ring index alone, so results are independent of other slots and of timing.
+// Work unit = (slot, head, chunk of kAttnChunk consecutive ring indices).  The kernel is
+// persistent: one CTA per SM walks the units u = blockIdx.x, + gridDim.x, ... and skips
+// chunks past a slot's n.  Per CTA:
+//   warp 8 lane 0   producer: bulk-copies each unit's K rows, V rows and the head's
+//                   query into a ring of shared-memory stages (mbarrier transaction
+//                   counts), so the HBM stream never waits on arithmetic;
+//   warps 0-3, 4-7  two consumer warpgroups taking alternate units.  Each warp scores
+//                   32 keys (4 lanes per key, 16-byte pieces XOR-swizzled by key parity
+//                   so that a quarter-warp's shared loads hit distinct banks), then
+//                   accumulates p.V with each lane owning Dh/32 output dims.  The four
+//                   warp partials are merged in warp order into the chunk partial
+//                   (max, sum, unnormalised output), written to global scratch; the
+//                   last unit of a (slot, head) to finish merges the chunks in chunk
+//                   order.
+// Every reduction order is fixed by ring index alone, so a slot's result does not depend
+// on the other slots, on the grid or on timing.
 #include <math.h>
 
+#include "pp_async.cuh"
+#include "pp_attn_common.cuh"
 #include "pp_internal.cuh"
 
 namespace pp {
 
 namespace {
 
-__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
+using namespace attn;
+
+constexpr int kConsumerWarps = 8;                      // each takes 16 keys of a unit
+constexpr int kKeysPerWarp = kAttnChunk / kConsumerWarps;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;
+constexpr int kAttnThreads = (kConsumerWarps + 2) * 32;
+constexpr int kPartSlots = 4;                          // warp-partial slots in flight
+static_assert(kKeysPerWarp % 8 == 0, "8 keys per score iteration");
+
+template <int DH>
+struct AttnCfg {
+  static constexpr int kKVBytes = kAttnChunk * DH * 2;          // K (or V) rows of one unit
+  static constexpr int kStageBytes = 2 * kKVBytes + DH * 4;     // K, V, fp32 query
+  static constexpr int kWarpPart = DH + 4;                      // m, l, -, -, o[DH] (floats)
+  static constexpr int kSlotBytes = kConsumerWarps * kWarpPart * 4;
+  static constexpr int kStagesRaw = (196 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  // stages | warp-partial slots | p [8][16] | barriers | flags
+  static constexpr int kSlotOff = kStages * kStageBytes;
+  static constexpr int kPOff = kSlotOff + kPartSlots * kSlotBytes;
+  static constexpr int kBarOff = kPOff + kConsumerWarps * kKeysPerWarp * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 * kPartSlots;
+  static constexpr int kFlagOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmem = kFlagOff + 16;
+  static_assert(kStages >= 2, "attention stage does not fit shared memory");
+  static_assert(kSmem <= 227 * 1024, "attention shared memory");
+  static_assert(kStageBytes % 16 == 0 && kSlotBytes % 16 == 0, "16-byte alignment");
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "r"(addr));
   return v;
 }
 
@@ -37,188 +78,337 @@ __device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
   }
 }
 
-template <int DH>
-__global__ void __launch_bounds__(kAttnWarps * 32, 4) k_attn(AttnArgs a) {
-  pdl_wait_and_trigger();
-  constexpr int PIECES = DH / 8;        // 16-byte pieces per K/V row
-  constexpr int LOADS = PIECES / 4;     // pieces per lane (4 lanes per key)
-  constexpr int ITER = 32 / 8;          // 8 keys per warp iteration, 32 keys per warp
-  static_assert(PIECES % 4 == 0, "head dim must be a multiple of 32");
-  const int c = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, qd = lane & 3;
-  const int HD = a.H * DH;
-  float* o_out = a.out + (size_t)s * a.out_ld + h * DH;
+// DPL consecutive bf16 values at a 2*DPL-byte aligned shared address, as fp32.
+template <int DPL>
+__device__ __forceinline__ void lds_dims(const uint16_t* p, float f[DPL]) {
+  if constexpr (DPL == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  } else if constexpr (DPL == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = __uint_as_float(w << 16);
+    f[1] = __uint_as_float(w & 0xFFFF0000u);
+  } else {
+    f[0] = __uint_as_float((uint32_t)*p << 16);
+  }
+}
 
-  const int n = min(a.n_valid[s], a.W);   // never read past the W ring positions
-  if (n <= 0) {   // closed slot: zero output
-    if (c == 0)
-      for (int i = threadIdx.x; i < DH; i += blockDim.x) {
-        o_out[i] = 0.f;
-        if (a.op) op_store(a.op, HD, a.op_Bp, s, h * DH + i, 0.f);
+// DPL floats at a 4*DPL-byte aligned address (shared or global)
+template <int DPL>
+__device__ __forceinline__ void ld_f(const float* p, float f[DPL]) {
+  if constexpr (DPL == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+  } else if constexpr (DPL == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(p);
+    f[0] = x.x; f[1] = x.y;
+  } else {
+    f[0] = *p;
+  }
+}
+template <int DPL>
+__device__ __forceinline__ void st_f(float* p, const float f[DPL]) {
+  if constexpr (DPL == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  } else if constexpr (DPL == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+  } else {
+    *p = f[0];
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units) {
+  using C = AttnCfg<DH>;
+  constexpr int S = C::kStages;
+  constexpr int PIECES = DH / 8;        // 16-byte pieces per K row
+  constexpr int LOADS = PIECES / 4;     // pieces per lane (4 lanes per key)
+  constexpr int DPL = DH / 32;          // output dims per lane in p.V and in the merges
+  constexpr int ITER = kKeysPerWarp / 8;
+  static_assert(PIECES % 4 == 0, "head dim must be a multiple of 32");
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* s_slot = reinterpret_cast<float*>(smem + C::kSlotOff);
+  float* s_p = reinterpret_cast<float*>(smem + C::kPOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  // bars: [0,S) K+q full | [S,2S) V full | [2S,3S) stage empty | [3S,3S+P) slot full |
+  //       [3S+P,3S+2P) slot empty
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kFlagOff);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t blk = (size_t)a.W * DH;
+  // this CTA's contiguous range of units
+  const int u0 = (int)(((long long)blockIdx.x * units) / gridDim.x);
+  const int u1 = (int)(((long long)(blockIdx.x + 1) * units) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(bar(i), 1);
+      mbar_init(bar(S + i), 1);
+      mbar_init(bar(2 * S + i), kConsumerWarps);
+    }
+    for (int i = 0; i < kPartSlots; ++i) {
+      mbar_init(bar(3 * S + i), kConsumerWarps);
+      mbar_init(bar(3 * S + kPartSlots + i), 1);
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait_and_trigger();
+
+  if (warp == kProducerWarp) {
+    // ---- producer -----------------------------------------------------------------
+    if (lane == 0) {
+      int v = 0;
+      for (int u = u0; u < u1; ++u) {
+        const Unit t = decode_unit(a, u);
+        if (t.nk == 0) continue;
+        const int st = v % S;
+        if (v >= S && !mbar_wait(bar(2 * S + st), ((v / S) - 1) & 1)) raise_timeout(a, s_abort);
+        if (*s_abort) break;
+        uint8_t* sk = smem + st * C::kStageBytes;
+        const size_t off = (size_t)t.s * a.slot_stride + t.h * blk + (size_t)t.c * kAttnChunk * DH;
+        const uint32_t bytes = (uint32_t)t.nk * DH * 2;
+        mbar_expect_tx(bar(st), bytes + DH * 4);
+        bulk_load(smem_u32(sk), a.k + off, bytes, bar(st));
+        bulk_load(smem_u32(sk + 2 * C::kKVBytes), a.q + (size_t)t.s * a.q_ld + t.h * DH, DH * 4,
+                  bar(st));
+        mbar_expect_tx(bar(S + st), bytes);
+        bulk_load(smem_u32(sk + C::kKVBytes), a.v + off, bytes, bar(S + st));
+        ++v;
       }
+      // every copy this CTA issued lands before the CTA may exit (bounded waits)
+      for (int i = v > S ? v - S : 0; i < v; ++i) {
+        mbar_wait(bar(i % S), (i / S) & 1);
+        mbar_wait(bar(S + i % S), (i / S) & 1);
+      }
+    }
     return;
   }
-  const int nc = (n + kAttnChunk - 1) / kAttnChunk;
-  if (c >= nc) return;
 
-  const size_t blk = (size_t)a.W * DH;
-  const uint16_t* Kh = a.k + (size_t)s * a.slot_stride + h * blk;
-  const uint16_t* Vh = a.v + (size_t)s * a.slot_stride + h * blk;
-
-  float q[LOADS][8];
-  const float* qp = a.q + (size_t)s * a.q_ld + h * DH;
+  if (warp == kEpilogueWarp) {
+    // ---- epilogue: warp partials -> chunk partial; tickets; final merges -----------
+    const int HD = a.H * DH;
+    int v = 0, run_pair = -1, run_len = 0, run_nc = 0;
+    auto flush = [&]() {   // this CTA's chunks of run_pair are all written
+      if (run_len == 0) return;
+      __syncwarp();
+      unsigned last = 0;
+      if (lane == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(a.count + run_pair, (unsigned)run_len);
+        last = (prev + (unsigned)run_len == (unsigned)run_nc);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        const int s = run_pair / a.H, h = run_pair - s * a.H;
+        merge_pair<DH>(a, a.part + (size_t)run_pair * attn_pair_floats(a.nc_max, DH), run_nc, s,
+                       h, lane);
+        if (lane == 0) a.count[run_pair] = 0u;
+      }
+      run_len = 0;
+    };
+    for (int u = u0; u < u1; ++u) {
+      const Unit t = decode_unit(a, u);
+      const int pair = t.s * a.H + t.h;
+      if (t.nk == 0) {
+        if (t.c == 0) {   // closed slot: zero output
+          for (int i = lane; i < DH; i += 32) {
+            a.out[(size_t)t.s * a.out_ld + t.h * DH + i] = 0.f;
+            if (a.op) op_store(a.op, HD, a.op_Bp, t.s, t.h * DH + i, 0.f);
+          }
+        }
+        continue;
+      }
+      if (pair != run_pair) {
+        flush();
+        run_pair = pair;
+        run_nc = (min(__ldg(a.n_valid + t.s), a.W) + kAttnChunk - 1) / kAttnChunk;
+      }
+      const int ps = v % kPartSlots;
+      const uint32_t ph = (v / kPartSlots) & 1;
+      ++v;
+      if (!*s_abort && !mbar_wait(bar(3 * S + ps), ph)) raise_timeout(a, s_abort);
+      const float* slot = s_slot + ps * (kConsumerWarps * C::kWarpPart);
+      float mw[kConsumerWarps];
+      float M = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < LOADS; ++j) {
-    const float4* p4 = reinterpret_cast<const float4*>(qp + (j * 4 + qd) * 8);
-    const float4 a0 = p4[0], a1 = p4[1];
-    q[j][0] = a0.x; q[j][1] = a0.y; q[j][2] = a0.z; q[j][3] = a0.w;
-    q[j][4] = a1.x; q[j][5] = a1.y; q[j][6] = a1.z; q[j][7] = a1.w;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        mw[w] = slot[w * C::kWarpPart];
+        M = fmaxf(M, mw[w]);
+      }
+      float L = 0.f, O[DPL];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) O[i] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {   // warp order
+        const float f = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - M);
+        float ow[DPL];
+        ld_f<DPL>(slot + w * C::kWarpPart + 4 + lane * DPL, ow);
+        L = fmaf(f, slot[w * C::kWarpPart + 1], L);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) O[i] = fmaf(f, ow[i], O[i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(3 * S + kPartSlots + ps));   // slot free
+      float* dst = a.part + (size_t)pair * attn_pair_floats(a.nc_max, DH) +
+                   (size_t)t.c * attn_rec_floats(DH);
+      if (lane < 8) dst[lane] = lane == 0 ? M : (lane == 1 ? L : 0.f);   // whole sector
+      st_f<DPL>(dst + 8 + lane * DPL, O);
+      ++run_len;
+    }
+    flush();
+    pdl_trigger();
+    return;
   }
 
-  const int key0 = c * kAttnChunk + warp * 32;
-  uint4 kr[ITER][LOADS];
-#pragma unroll
-  for (int it = 0; it < ITER; ++it) {
-    const int key = key0 + it * 8 + g;
-#pragma unroll
-    for (int j = 0; j < LOADS; ++j)
-      kr[it][j] = (key < n) ? ld_stream(Kh + (size_t)key * DH + (j * 4 + qd) * 8)
-                            : make_uint4(0, 0, 0, 0);
-  }
-  float sc[ITER];
-#pragma unroll
-  for (int it = 0; it < ITER; ++it) {
-    float dot = 0.f;
+  // ---- consumers: warp w scores keys w*16 .. w*16+15 of each unit, then p.V --------
+  const int g = lane >> 2, qd = lane & 3;
+  const int par = (LOADS >= 2) ? (g & 1) : 0;   // piece swizzle of this lane's key
+  float* pw = s_p + warp * kKeysPerWarp;
+  const int key0 = warp * kKeysPerWarp;
+  int v = 0;
+  for (int u = u0; u < u1; ++u) {
+    const Unit t = decode_unit(a, u);
+    if (t.nk == 0) continue;
+    const int st = v % S, ps = v % kPartSlots;
+    const uint32_t ph = (v / S) & 1;
+    const bool reuse_slot = v >= kPartSlots;
+    const uint32_t pph = ((v / kPartSlots) - 1) & 1;
+    ++v;
+    const uint8_t* sk = smem + st * C::kStageBytes;
+    const uint32_t k_base = smem_u32(sk);
+    const uint16_t* vs = reinterpret_cast<const uint16_t*>(sk + C::kKVBytes);
+    const float* qs = reinterpret_cast<const float*>(sk + 2 * C::kKVBytes);
+    const int kcount = max(0, min(kKeysPerWarp, t.nk - key0));
+
+    if (!*s_abort && !mbar_wait(bar(st), ph)) raise_timeout(a, s_abort);
+    // scores: lane (g, qd) holds pieces (j ^ par) * 4 + qd of the query and of its key
+    float q[LOADS][8];
 #pragma unroll
     for (int j = 0; j < LOADS; ++j) {
-      float kf[8];
-      unpack8(kr[it][j], kf);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) dot = fmaf(q[j][t], kf[t], dot);
+      const float4* p4 = reinterpret_cast<const float4*>(qs + (((j ^ par) * 4 + qd) * 8));
+      const float4 a0 = p4[0], a1 = p4[1];
+      q[j][0] = a0.x; q[j][1] = a0.y; q[j][2] = a0.z; q[j][3] = a0.w;
+      q[j][4] = a1.x; q[j][5] = a1.y; q[j][6] = a1.z; q[j][7] = a1.w;
     }
-    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-    sc[it] = (key0 + it * 8 + g < n) ? dot * a.q_scale : -INFINITY;
-  }
-  float m = sc[0];
-#pragma unroll
-  for (int it = 1; it < ITER; ++it) m = fmaxf(m, sc[it]);
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-
-  __shared__ float sm_m[kAttnWarps], sm_l[kAttnWarps];
-  __shared__ float sm_o[kAttnWarps][DH];
-  __shared__ int sm_last;
-
-  float l = 0.f;
-  float acc[LOADS][8];
-#pragma unroll
-  for (int j = 0; j < LOADS; ++j)
-#pragma unroll
-    for (int t = 0; t < 8; ++t) acc[j][t] = 0.f;
-  if (m != -INFINITY) {   // warp-uniform: this warp has at least one valid key
-    float p[ITER];
-#pragma unroll
-    for (int it = 0; it < ITER; ++it) {
-      p[it] = (sc[it] == -INFINITY) ? 0.f : exp2f(sc[it] - m);
-      l += p[it];
-    }
-    uint4 vr[ITER][LOADS];
+    float sc[ITER];
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
       const int key = key0 + it * 8 + g;
+      uint4 kr[LOADS];
 #pragma unroll
       for (int j = 0; j < LOADS; ++j)
-        vr[it][j] = (key < n) ? ld_stream(Vh + (size_t)key * DH + (j * 4 + qd) * 8)
-                              : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int it = 0; it < ITER; ++it) {
+        kr[j] = lds128(k_base + (uint32_t)(key * DH + ((j ^ par) * 4 + qd) * 8) * 2);
+      float dot = 0.f;
 #pragma unroll
       for (int j = 0; j < LOADS; ++j) {
-        float vf[8];
-        unpack8(vr[it][j], vf);
+        float kf[8];
+        unpack8(kr[j], kf);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) acc[j][t] = fmaf(p[it], vf[t], acc[j][t]);
+        for (int e = 0; e < 8; ++e) dot = fmaf(q[j][e], kf[e], dot);
+      }
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      sc[it] = (key < t.nk) ? dot * a.q_scale : -INFINITY;
+    }
+    float m = sc[0];
+#pragma unroll
+    for (int it = 1; it < ITER; ++it) m = fmaxf(m, sc[it]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+
+    float l = 0.f;
+    float acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    if (!*s_abort && !mbar_wait(bar(S + st), ph)) raise_timeout(a, s_abort);
+    if (kcount > 0) {   // warp-uniform
+#pragma unroll
+      for (int it = 0; it < ITER; ++it) {
+        const float p = (sc[it] == -INFINITY) ? 0.f : exp2f(sc[it] - m);
+        l += p;
+        if (qd == 0) pw[it * 8 + g] = p;
+      }
+      __syncwarp();
+      // p.V in key order; lane owns dims lane*DPL .. +DPL
+      const uint16_t* vrow = vs + key0 * DH + lane * DPL;
+      int k = 0;
+      for (; k + 8 <= kcount; k += 8) {
+        float vf[8][DPL];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) lds_dims<DPL>(vrow + (k + e) * DH, vf[e]);
+        const float4 p0 = *reinterpret_cast<const float4*>(pw + k);
+        const float4 p1 = *reinterpret_cast<const float4*>(pw + k + 4);
+        const float pk[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) acc[i] = fmaf(pk[e], vf[e][i], acc[i]);
+      }
+      for (; k < kcount; ++k) {
+        float vf[DPL];
+        lds_dims<DPL>(vrow + k * DH, vf);
+        const float pk = pw[k];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(pk, vf[i], acc[i]);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(2 * S + st));   // stage free
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    // warp partial into the unit's slot
+    if (reuse_slot && !*s_abort && !mbar_wait(bar(3 * S + kPartSlots + ps), pph))
+      raise_timeout(a, s_abort);
+    float* wp = s_slot + ps * (kConsumerWarps * C::kWarpPart) + warp * C::kWarpPart;
+    if (lane == 0) { wp[0] = m; wp[1] = l; }
+    st_f<DPL>(wp + 4 + lane * DPL, acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(3 * S + ps));
   }
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l += __shfl_xor_sync(0xffffffffu, l, o);
-#pragma unroll
-    for (int j = 0; j < LOADS; ++j)
-#pragma unroll
-      for (int t = 0; t < 8; ++t) acc[j][t] += __shfl_xor_sync(0xffffffffu, acc[j][t], o);
-  }
-  if (lane == 0) { sm_m[warp] = m; sm_l[warp] = l; }
-  if (g == 0) {
-#pragma unroll
-    for (int j = 0; j < LOADS; ++j)
-#pragma unroll
-      for (int t = 0; t < 8; ++t) sm_o[warp][(j * 4 + qd) * 8 + t] = acc[j][t];
-  }
-  __syncthreads();
+}
 
-  // chunk partial: merge the warps in warp order
-  float* part = a.part + (((size_t)s * a.H + h) * a.nc_max) * (DH + 2);
-  {
-    float M = sm_m[0];
-    for (int w = 1; w < kAttnWarps; ++w) M = fmaxf(M, sm_m[w]);
-    for (int i = threadIdx.x; i < DH + 1; i += blockDim.x) {
-      float v = 0.f;
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float f = (sm_m[w] == -INFINITY) ? 0.f : exp2f(sm_m[w] - M);
-        v = fmaf(f, (i < DH) ? sm_o[w][i] : sm_l[w], v);
-      }
-      float* dst = part + (size_t)c * (DH + 2);
-      if (i < DH) dst[2 + i] = v; else dst[1] = v;
-      if (i == 0) dst[0] = M;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  pdl_trigger();   // this chunk is done: the next kernel may start launching
-  if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(a.count + (size_t)s * a.H + h, 1u);
-    sm_last = (prev == (unsigned)(nc - 1));
-  }
-  __syncthreads();
-  if (!sm_last) return;
-  __threadfence();
-
-  // last CTA: merge the chunks in chunk order
-  float M = -INFINITY;
-  for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, __ldcg(part + (size_t)cc * (DH + 2)));
-  for (int i = threadIdx.x; i < DH; i += blockDim.x) {
-    float L = 0.f, O = 0.f;
-    for (int cc = 0; cc < nc; ++cc) {
-      const float* src = part + (size_t)cc * (DH + 2);
-      const float f = exp2f(__ldcg(src) - M);
-      L = fmaf(f, __ldcg(src + 1), L);
-      O = fmaf(f, __ldcg(src + 2 + i), O);
-    }
-    o_out[i] = O / L;
-    if (a.op) op_store(a.op, HD, a.op_Bp, s, h * DH + i, O / L);
-  }
-  if (threadIdx.x == 0) a.count[(size_t)s * a.H + h] = 0u;
+template <int DH>
+cudaError_t launch_dh(const AttnArgs& a, int B, cudaStream_t s) {
+  using C = AttnCfg<DH>;
+  cudaError_t err =
+      cudaFuncSetAttribute(k_attn<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (err != cudaSuccess) return err;
+  const int units = B * a.H * a.nc_max;
+  const int nsm = attn::sm_count();
+  const int grid = units < nsm ? units : nsm;
+  return launch_k(k_attn<DH>, dim3(grid), dim3(kAttnThreads), (size_t)C::kSmem, s, 1, a, units);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, cudaStream_t s) {
-  const dim3 grid(a.nc_max, a.H, B);
+cudaError_t launch_attn_cc(const AttnArgs& a, int B, int Dh, cudaStream_t s) {
+  if (B < 1 || a.H < 1 || a.nc_max < 1) return cudaErrorInvalidValue;
   switch (Dh) {
-    case 32: return launch_k(k_attn<32>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
-    case 64: return launch_k(k_attn<64>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
-    case 128: return launch_k(k_attn<128>, grid, dim3(kAttnWarps * 32), 0, s, 1, a);
+    case 32: return launch_dh<32>(a, B, s);
+    case 64: return launch_dh<64>(a, B, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, const AttnMaps* maps,
+                             int slot_base, cudaStream_t s) {
+  if (Dh == 128) {
+    if (!maps || !a.q_op) return cudaErrorInvalidValue;
+    return launch_attn_tc(a, B, *maps, slot_base, s);
+  }
+  return launch_attn_cc(a, B, Dh, s);
+}
+
 // The tick's attention for one layer: the slot's rotated, pre-scaled q against its ring.
-cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s) {
+cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, const AttnMaps* maps,
+                        cudaStream_t s) {
   AttnArgs a{};
   a.q = b.q;
   a.q_ld = D.d;
@@ -237,7 +427,10 @@ cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cud
   a.op_Bp = D.Bp;
   a.part = b.attn_part;
   a.count = b.attn_count;
-  return launch_attn_args(a, D.B, D.Dh, s);
+  a.status = b.status;
+  a.q_op = b.q_op;
+  // the K/V maps span every layer's ring: slot coordinate = layer * B + slot
+  return launch_attn_args(a, D.B, D.Dh, maps, layer * D.B, s);
 }
 
 }  // namespace pp

@@ -22,11 +22,14 @@ constexpr int kNoAllocMaxPairs = 2048;
 constexpr int kNoAllocMaxWindow = 3072;
 constexpr int kNoAllocMaxHeadDim = 128;
 constexpr size_t kNoAllocPartBytes =
-    (((size_t)kNoAllocMaxPairs * (kNoAllocMaxWindow / kAttnChunk) * (kNoAllocMaxHeadDim + 2) *
-      sizeof(float)) + 255) & ~(size_t)255;
-constexpr size_t kNoAllocBytes = kNoAllocPartBytes + (size_t)kNoAllocMaxPairs * sizeof(uint32_t);
+    (((size_t)kNoAllocMaxPairs *
+      attn_pair_floats(kNoAllocMaxWindow / kAttnChunk, kNoAllocMaxHeadDim) * sizeof(float)) +
+     255) & ~(size_t)255;
+constexpr size_t kNoAllocCountBytes = (size_t)kNoAllocMaxPairs * sizeof(uint32_t);
+constexpr size_t kNoAllocQopBytes = (size_t)kNoAllocMaxPairs * 2 * kNoAllocMaxHeadDim * 2;
+constexpr size_t kNoAllocBytes = kNoAllocPartBytes + kNoAllocCountBytes + kNoAllocQopBytes;
 
-// Every GPU that loads the library holds this array (about 12.2 MiB) until exit.
+// Every GPU that loads the library holds this array (about 25.4 MiB) until exit.
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -87,11 +90,19 @@ extern "C" int pp_ring_attention_noalloc(const float* q, const uint16_t* k, cons
   a.out = out;
   a.out_ld = H * head_dim;
   a.op = nullptr;
-  a.part = reinterpret_cast<float*>(base);
-  a.count = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(base) + kNoAllocPartBytes);
+  char* sp = reinterpret_cast<char*>(base);
+  a.part = reinterpret_cast<float*>(sp);
+  a.count = reinterpret_cast<uint32_t*>(sp + kNoAllocPartBytes);
+  AttnMaps maps;
+  if (head_dim == 128) {
+    a.q_op = reinterpret_cast<uint16_t*>(sp + kNoAllocPartBytes + kNoAllocCountBytes);
+    if (!attn_maps(&maps, k, v, (size_t)slot_stride, B, H, window, head_dim, a.q_op, B * H))
+      return PP_EINVAL;
+  }
   cudaStream_t s = (cudaStream_t)stream;
   // the array keeps the previous call's contents: the tickets must start at zero
   cudaError_t err = cudaMemsetAsync(a.count, 0, (size_t)B * H * sizeof(uint32_t), s);
-  if (err == cudaSuccess) err = launch_attn_args(a, B, head_dim, s);
+  if (err == cudaSuccess && head_dim == 128) err = launch_q_split(a, B, head_dim, s);
+  if (err == cudaSuccess) err = launch_attn_args(a, B, head_dim, &maps, 0, s);
   return err == cudaSuccess ? PP_OK : PP_E_CUDA;
 }

@@ -174,8 +174,13 @@ __global__ void k_rope_ring(Dims D, Buffers b, int layer) {
   const float v0 = row[2 * D.d], v1 = row[2 * D.d + 1];
   const float qs = 1.4426950408889634f / sqrtf((float)D.Dh);
   float* q = b.q + (size_t)s * D.d + h * D.Dh + 2 * i;
-  q[0] = (q0 * c - q1 * sn) * qs;
-  q[1] = (q0 * sn + q1 * c) * qs;
+  const float qr0 = (q0 * c - q1 * sn) * qs, qr1 = (q0 * sn + q1 * c) * qs;
+  q[0] = qr0;
+  q[1] = qr1;
+  // the same query as the bf16 hi/lo operand rows of the tensor-core attention
+  uint16_t* qo = b.q_op + ((size_t)(s * D.H + h) * 2) * D.Dh + 2 * i;
+  bf16_split(qr0, qo[0], qo[D.Dh]);
+  bf16_split(qr1, qo[1], qo[D.Dh + 1]);
   const float kr0 = k0 * c - k1 * sn, kr1 = k0 * sn + k1 * c;
   const size_t blk = (size_t)D.W * D.Dh;
   const size_t kbase = ((((size_t)layer * D.B + s) * 2 + 0) * D.H + h) * blk;

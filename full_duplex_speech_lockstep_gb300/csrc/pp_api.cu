@@ -56,6 +56,8 @@ struct Group {
   Dims D;
   Buffers buf;
   Mm mm[MM_COUNT];
+  AttnMaps amaps;        // ring and query operand maps of the tensor-core attention
+  bool has_amaps = false;
 };
 
 struct pp_engine {
@@ -184,10 +186,11 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.z = cv.take<float>(Bs * D.d);
     b.qkv = cv.take<float>(Bs * 3 * D.d);
     b.q = cv.take<float>(Bs * D.d);
+    b.q_op = cv.take<uint16_t>(Bs * D.H * 2 * D.Dh);
     b.o = cv.take<float>(Bs * D.d);
     b.hmlp = cv.take<float>(Bs * D.F);
     b.rope_cs = cv.take<float>(Bs * D.Dh);
-    b.attn_part = cv.take<float>(Bs * D.H * D.nc_max * (D.Dh + 2));
+    b.attn_part = cv.take<float>(Bs * D.H * attn_pair_floats(D.nc_max, D.Dh));
     b.tok = cv.take<int32_t>(Bs);
     b.y = cv.take<float>(Bs * D.dd);
     b.yn = cv.take<float>(Bs * dwide);
@@ -254,6 +257,37 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t k, uint3
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+}  // namespace
+
+// K and V as 4-D [slots][H][W][Dh] (slot stride in elements), box 64 dims x 128 ring rows;
+// the query operand as 2-D [pairs*2][Dh], box 64 x 2 rows.  Rows past W (or past the
+// last query row) read as zero.
+bool pp::attn_maps(AttnMaps* m, const uint16_t* k, const uint16_t* v, size_t slot_stride, int slots,
+               int H, int W, int Dh, const uint16_t* q_op, int pairs) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || Dh != 128) return false;
+  cuuint64_t gdim[4] = {(cuuint64_t)Dh, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)slots};
+  cuuint64_t gstride[3] = {(cuuint64_t)Dh * 2, (cuuint64_t)W * Dh * 2, (cuuint64_t)slot_stride * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kAttnChunk, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    if (fn(i == 0 ? &m->k : &m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+           const_cast<uint16_t*>(i == 0 ? k : v), gdim, gstride, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  cuuint64_t qdim[2] = {(cuuint64_t)Dh, (cuuint64_t)pairs * 2};
+  cuuint64_t qstride[1] = {(cuuint64_t)Dh * 2};
+  cuuint32_t qbox[2] = {64, 2};   // rows hi, lo of one (slot, head); the other operand rows
+                                  // of the MMA tile feed output columns that are never read
+  return fn(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(q_op), qdim, qstride,
+            qbox, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 // K-splits per M-tile: a function of the matrix shape and the device's SM count only,
 // never of the batch, so every engine size reduces in the same order.  Model: units run
@@ -382,7 +416,7 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     MARK(PP_K_ROPE_RING);
     PP_TRY(launch_rope_ring(D, b, l, s));
     MARK(PP_K_ATTN);
-    PP_TRY(launch_attn(D, b, l, true, s));
+    PP_TRY(launch_attn(D, b, l, true, e->has_amaps ? &e->amaps : nullptr, s));
     NormIO on;
     on.alpha_out = b.mlp_alpha + (size_t)l * D.d;
     on.op_next = b.op_d;
@@ -478,7 +512,8 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
 
 // The tick with the CUDA-core contractions.  With prof != nullptr a timing event is
 // recorded before every launch (and once at the end).
-cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Prof* prof) {
+cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, const AttnMaps* amaps, cudaStream_t s,
+                            Prof* prof) {
   MARK(PP_K_BEGIN);
   PP_TRY(launch_begin(D, b, nullptr, nullptr, nullptr, s));
   for (int l = 0; l < D.L; ++l) {
@@ -492,7 +527,7 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
     MARK(PP_K_ROPE_RING);
     PP_TRY(launch_rope_ring(D, b, l, s));
     MARK(PP_K_ATTN);
-    PP_TRY(launch_attn(D, b, l, false, s));
+    PP_TRY(launch_attn(D, b, l, false, amaps, s));
     a = GemvArgs{};
     a.W = b.wo + (size_t)l * D.d * D.d; a.M = D.d; a.K = D.d;
     a.X = b.o; a.ldx = D.d; a.Y = b.x; a.ldy = D.d; a.epi = EPI_ADD;
@@ -582,7 +617,9 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, cudaStream_t s, Pro
 cudaError_t enqueue_group(const pp_engine* e, int g, cudaStream_t s, Prof* prof) {
   g_launch_priority = 0;
   cudaError_t err = e->tensor ? enqueue_tick_tensor(&e->grp[g], e->dep_priority, s, prof)
-                              : enqueue_tick_cc(e->grp[g].D, e->grp[g].buf, s, prof);
+                              : enqueue_tick_cc(e->grp[g].D, e->grp[g].buf,
+                                                e->grp[g].has_amaps ? &e->grp[g].amaps : nullptr,
+                                                s, prof);
   g_launch_priority = 0;
   return err;
 }
@@ -718,6 +755,16 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
       char* op_lo = reinterpret_cast<char*>(b.op_d);
       char* op_hi = reinterpret_cast<char*>(b.op_fd + 2 * (size_t)D.Bp * D.Fd);
       err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
+    }
+  }
+  for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+    Group* gr = &e->grp[g];
+    const Dims& D = gr->D;
+    if (D.Dh == 128) {   // the tensor-core attention reads the ring through tensor maps
+      const size_t blk = (size_t)D.H * D.W * D.Dh;
+      gr->has_amaps = attn_maps(&gr->amaps, gr->buf.ring, gr->buf.ring + blk, 2 * blk, D.L * D.B,
+                                D.H, D.W, D.Dh, gr->buf.q_op, D.B * D.H);
+      if (!gr->has_amaps) err = cudaErrorInvalidValue;
     }
   }
   if (err == cudaSuccess && e->tensor) {
@@ -943,12 +990,20 @@ static bool ring_attention_args_ok(int B, int H, int head_dim, int window) {
 
 static size_t ring_attention_part_bytes(int B, int H, int head_dim, int window) {
   const size_t nc = (size_t)(window + kAttnChunk - 1) / kAttnChunk;
-  return (((size_t)B * H * nc * (head_dim + 2) * sizeof(float)) + 255) & ~(size_t)255;
+  return (((size_t)B * H * attn_pair_floats((int)nc, head_dim) * sizeof(float)) + 255) &
+         ~(size_t)255;
+}
+
+static size_t ring_attention_count_bytes(int B, int H) {
+  return ((size_t)B * H * sizeof(uint32_t) + 255) & ~(size_t)255;
 }
 
 size_t pp_ring_attention_scratch_bytes(int B, int H, int head_dim, int window) {
   if (!ring_attention_args_ok(B, H, head_dim, window)) return 0;
-  return ring_attention_part_bytes(B, H, head_dim, window) + (size_t)B * H * sizeof(uint32_t);
+  // partials | tickets | (head dim 128) the bf16 hi/lo query operand
+  const size_t qop = head_dim == 128 ? (size_t)B * H * 2 * head_dim * sizeof(uint16_t) : 0;
+  return ring_attention_part_bytes(B, H, head_dim, window) + ring_attention_count_bytes(B, H) +
+         qop;
 }
 
 int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int64_t slot_stride,
@@ -975,12 +1030,21 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
   a.out = out;
   a.out_ld = H * head_dim;
   a.op = nullptr;
-  a.part = reinterpret_cast<float*>(scratch);
-  a.count = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(scratch) +
-                                        ring_attention_part_bytes(B, H, head_dim, window));
+  char* sp = reinterpret_cast<char*>(scratch);
+  a.part = reinterpret_cast<float*>(sp);
+  sp += ring_attention_part_bytes(B, H, head_dim, window);
+  a.count = reinterpret_cast<uint32_t*>(sp);
+  sp += ring_attention_count_bytes(B, H);
+  AttnMaps maps;
+  if (head_dim == 128) {
+    a.q_op = reinterpret_cast<uint16_t*>(sp);
+    if (!attn_maps(&maps, k, v, (size_t)slot_stride, B, H, window, head_dim, a.q_op, B * H))
+      return PP_EINVAL;
+  }
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t err = cudaMemsetAsync(a.count, 0, (size_t)B * H * sizeof(uint32_t), s);
-  if (err == cudaSuccess) err = launch_attn_args(a, B, head_dim, s);
+  if (err == cudaSuccess && head_dim == 128) err = launch_q_split(a, B, head_dim, s);
+  if (err == cudaSuccess) err = launch_attn_args(a, B, head_dim, &maps, 0, s);
   return err == cudaSuccess ? PP_OK : PP_E_CUDA;
 }
 

@@ -9,8 +9,15 @@
 namespace pp {
 
 constexpr int kRows = PP_ROWS;
-constexpr int kAttnChunk = 256;     // ring positions per attention CTA (split-K unit)
-constexpr int kAttnWarps = 8;       // 32 positions per warp
+constexpr int kAttnChunk = 128;     // ring positions per attention work unit (split-K unit)
+
+// Chunk partial of the ring attention: [max, sum, 0 x 6, o[Dh]] floats, so that every
+// 32-byte sector is written whole; the records of one (slot, head) form a block padded
+// to 128 bytes (whole L2 lines, discarded once merged).
+__host__ __device__ constexpr int attn_rec_floats(int Dh) { return Dh + 8; }
+__host__ __device__ constexpr size_t attn_pair_floats(int nc_max, int Dh) {
+  return ((size_t)nc_max * (size_t)(Dh + 8) + 31) & ~(size_t)31;
+}
 constexpr int kMaxBatch = 64;
 
 // Device-side pointers and sizes every kernel of the tick needs.
@@ -66,10 +73,11 @@ struct Buffers {
   float* z;                // [B][d] post final norm (text head and depformer input)
   float* qkv;              // [B][3d]
   float* q;                // [B][d] rotated, pre-scaled query
+  uint16_t* q_op;          // [B][H][2][Dh] the same query as bf16 hi/lo rows
   float* o;                // [B][d]
   float* hmlp;             // [B][F]
   float* rope_cs;          // [B][Dh/2][2]
-  float* attn_part;        // [B][H][nc_max][Dh+2]
+  float* attn_part;        // [B][H] blocks of attn_pair_floats(nc_max, Dh)
   uint32_t* attn_count;    // [B][H]
   float* logits;           // [B][logits_ld]
   int32_t* tok;            // [B] token feeding the next depformer step
@@ -152,15 +160,23 @@ cudaError_t launch_begin(const Dims& D, const Buffers& b, const float* alpha, ui
 cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
                            float* out, int ldo, uint16_t* op, cudaStream_t s);
 
-// hi/lo split of v into operand row b (hi) and Bp + b (lo), column k
-__device__ __forceinline__ void op_store(uint16_t* op, int ld, int Bp, int b, int k, float v) {
+// hi = bf16(v) and lo = bf16(v - hi), both rounded to nearest even (NaN stays NaN)
+__device__ __forceinline__ void bf16_split(float v, uint16_t& hi, uint16_t& lo) {
   uint32_t u = __float_as_uint(v);
   uint32_t h = (u & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : ((u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u);
   const float rem = v - __uint_as_float(h);
   uint32_t r = __float_as_uint(rem);
   r = (r & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : r + 0x7FFFu + ((r >> 16) & 1u);
-  op[(size_t)b * ld + k] = (uint16_t)(h >> 16);
-  op[(size_t)(Bp + b) * ld + k] = (uint16_t)(r >> 16);
+  hi = (uint16_t)(h >> 16);
+  lo = (uint16_t)(r >> 16);
+}
+
+// hi/lo split of v into operand row b (hi) and Bp + b (lo), column k
+__device__ __forceinline__ void op_store(uint16_t* op, int ld, int Bp, int b, int k, float v) {
+  uint16_t hi, lo;
+  bf16_split(v, hi, lo);
+  op[(size_t)b * ld + k] = hi;
+  op[(size_t)(Bp + b) * ld + k] = lo;
 }
 
 // Tensor-core contraction (k_umma.cu).
@@ -233,11 +249,31 @@ struct AttnArgs {
   int out_ld;
   uint16_t* op;            // optional bf16 hi/lo operand [2*op_Bp][H*Dh]
   int op_Bp;
-  float* part;             // scratch [B*H][nc_max][Dh+2]
+  float* part;             // scratch [B*H] blocks of attn_pair_floats(nc_max, Dh)
   uint32_t* count;         // scratch [B*H], zero before the call; left zero after it
+  uint32_t* status;        // optional: PP_S_TIMEOUT is raised here when a wait gives up
+  uint16_t* q_op;          // head dim 128: bf16 hi/lo query operand [B*H*2][Dh], already
+                           // scaled by q_scale (the tensor-core kernel reads only this)
 };
-cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, cudaStream_t s);
-cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, cudaStream_t s);
+// Tensor maps of the tensor-core attention (head dim 128): K and V as 4-D [slot][H][W][Dh]
+// bf16 (box 64 x 128 rows), the query operand as 2-D [B*H*2][Dh] (box 64 x 2 rows),
+// all with the 128-byte swizzle.
+struct AttnMaps {
+  CUtensorMap k, v, q;
+};
+bool attn_maps(AttnMaps* m, const uint16_t* k, const uint16_t* v, size_t slot_stride, int slots,
+               int H, int W, int Dh, const uint16_t* q_op, int pairs);
+// Head dim 128 runs on the tensor cores (maps and a.q_op required; slot_base is the slot
+// coordinate of slot 0 in the K/V maps); head dims 32 and 64 run on the CUDA cores.
+cudaError_t launch_attn_args(const AttnArgs& a, int B, int Dh, const AttnMaps* maps,
+                             int slot_base, cudaStream_t s);
+cudaError_t launch_attn_cc(const AttnArgs& a, int B, int Dh, cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnArgs& a, int B, const AttnMaps& maps, int slot_base,
+                           cudaStream_t s);
+// q_op[(s*H + h)*2 + {0,1}][i] = hi/lo of q_scale * q[s][h*Dh + i]
+cudaError_t launch_q_split(const AttnArgs& a, int B, int Dh, cudaStream_t s);
+cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, const AttnMaps* maps,
+                        cudaStream_t s);
 cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
                             cudaStream_t s);

@@ -238,10 +238,15 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
  *   out[s][h*D + i] = sum_{j < n_valid[s]} softmax_j(q[s][h] . K_j / sqrt(D)) V_j[i]
  * over ring indices j (softmax does not depend on key order, so the ring need not be
  * rotated); n_valid[s] == 0 gives zeros.  Reductions run in a fixed order set by the
- * ring index alone, so every slot's result is independent of the others.
+ * ring index alone, so every slot's result is independent of the others.  D = 128 runs
+ * on the tensor cores: q / sqrt(D) and the softmax weights enter them as bf16 hi/lo
+ * pairs (about 16 significant bits; relative error ~1e-5 against fp64); D = 32 and 64
+ * run on the CUDA cores in fp32.
  *   q          f32 [B][H][D], device, 16-byte aligned
  *   k, v       bf16: head h of slot s is the [W][D] block at k + s*slot_stride + h*W*D
- *              (elements), device, 16-byte aligned, slot_stride a multiple of 8
+ *              (elements), device, 16-byte aligned, slot_stride a multiple of 8; for
+ *              D = 128 the blocks are read through a tensor map, and a layout the map
+ *              cannot describe returns PP_EINVAL
  *   n_valid    int32 [B], device; values above W count as W, values <= 0 give zeros
  *   out        f32 [B][H*D], device
  *   scratch    device memory of at least pp_ring_attention_scratch_bytes(B, H, D, W)
@@ -259,7 +264,7 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
  * (it can synchronise the device and take milliseconds) would break the 80 ms cadence.
  * The pages have no counterpart to this call; it exists for those callers.
  * Same arguments and result as pp_ring_attention, minus the scratch: the partials and
- * tickets live in one device array built into the library (about 12.2 MiB, held on
+ * tickets live in one device array built into the library (about 25.4 MiB, held on
  * every GPU that loads the library until the process exits).  Limits: B*H <= 2048,
  * window <= 3072, head_dim <= 128; larger sizes return PP_E_RANGE.  The first call on
  * a device looks up the array's device address (make that first call before any
