@@ -34,12 +34,12 @@ SEED = 5
 HBM_NOMINAL_GBS = 8000.0
 
 # DRAM traffic of the attention kernel from one ncu capture (profiles/
-# k_attn_b8_fullshape_2layers.md): dram__bytes_read + dram__bytes_write of one launch at
-# B=8 with a full 3000-position ring, per (slot, valid position).  Traffic grows in
+# k_attn_tc_b8_fullshape_2layers.md): dram__bytes_read + dram__bytes_write of one launch
+# at B=8 with a full 3000-position ring, per (slot, valid position).  Traffic grows in
 # proportion to the slots, so a full launch's traffic is this times slots x positions.
-# Valid only while k_attn.cu is the source that was captured (its hash below).
-ATTN_TRAFFIC = {"bytes_per_slot_position": (393.383168e6 + 4.116992e6) / (8 * 3000),
-                "source_sha256_16": "18f863747c5a8737"}
+# Valid only while k_attn_tc.cu is the source that was captured (its hash below).
+ATTN_TRAFFIC = {"bytes_per_slot_position": (394.677248e6 + 5.22368e6) / (8 * 3000),
+                "source_sha256_16": "90300a4a90da77f6"}
 
 
 def parse():
@@ -356,10 +356,10 @@ def main():
     attn_gbs = attn_bytes / (attn_ms / 1000.0) / 1e9 if kind_n[ia] else None
     traffic = None
     import hashlib
-    src = os.path.join(ROOT, "full_duplex_speech_lockstep_gb300", "csrc", "k_attn.cu")
+    src = os.path.join(ROOT, "full_duplex_speech_lockstep_gb300", "csrc", "k_attn_tc.cu")
     if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == ATTN_TRAFFIC["source_sha256_16"]:
         traffic = ATTN_TRAFFIC["bytes_per_slot_position"] * B * n_prof
-    roofline = {"kernel": "k_attn (split-K ring attention)", "bound": "hbm",
+    roofline = {"kernel": "k_attn_tc (tensor-core split-K ring attention)", "bound": "hbm",
                 "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
                 "frac": attn_gbs / hbm_peak if attn_gbs else None, "traffic": traffic,
                 "peak_source": peak_src, "bytes_per_launch": attn_bytes,

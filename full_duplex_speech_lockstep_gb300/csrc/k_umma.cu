@@ -69,6 +69,10 @@ struct Cfg {
   static constexpr int kStages = (96 * 1024) / kStageBytes < 8 ? (96 * 1024) / kStageBytes : 8;
   static constexpr int kTmemCols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, 1/rms*/;
+  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][129] floats, then
+  // the pushed slice sums [kMaxSplits][64] floats at 72 KB
+  static_assert(2 * (N / 2) * 129 * 4 <= 72 * 1024, "epilogue partials overlap the push area");
+  static_assert(72 * 1024 + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
 };
 
 template <int N>
@@ -325,6 +329,8 @@ __global__ void __launch_bounds__(128, 2)
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int S = a.splits;
+  // y^2 sums of each split's slice, pushed into rank 0's idle stage memory (fused RMSNorm)
+  float* s_push = reinterpret_cast<float*>(smem + 72 * 1024);   // [kMaxSplits][B]
   const float* peer[kMaxSplits];
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? cluster.map_shared_rank(mine, q) : mine;
@@ -367,10 +373,12 @@ __global__ void __launch_bounds__(128, 2)
         mrow[i] = (e < n) ? mt * 128 + rr : a.M;     // a.M marks "no element"
         off[i] = bcol[i] * PR + rr;
       }
-      float ex[CH];
+      float ex[CH], al[CH];   // residual (or embedding) and norm gain, loaded with the partials
 #pragma unroll
-      for (int i = 0; i < CH; ++i)
+      for (int i = 0; i < CH; ++i) {
         ex[i] = (a.epi != EPI_STORE && mrow[i] < a.M) ? epi_extra(a, bcol[i], mrow[i]) : 0.f;
+        al[i] = (norm_out && mrow[i] < a.M) ? a.norm_alpha[mrow[i]] : 0.f;
+      }
       float pv[CH][kMaxSplits];
 #pragma unroll
       for (int i = 0; i < CH; ++i)
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(128, 2)
           const float y = v + ex[i];
           a.Y[(size_t)bcol[i] * a.ldy + mrow[i]] = y;
           if (norm_out) {
-            op_store(a.norm_op, a.M, Bp, bcol[i], mrow[i], a.norm_alpha[mrow[i]] * y);
+            op_store(a.norm_op, a.M, Bp, bcol[i], mrow[i], al[i] * y);
             sq[off[i] - r0] = y * y;
           }
         } else if (norm_out && e < n) {
@@ -397,24 +405,20 @@ __global__ void __launch_bounds__(128, 2)
         }
       }
     }
-    if (norm_out) {   // this slice's sums of y^2, in row order, parked for CTA 0 of the tile
+    if (norm_out) {   // this slice's sums of y^2, in row order, pushed to rank 0 of the tile
       __syncthreads();
       if (threadIdx.x < B) {
         float ss = 0.f;
         for (int rr = 0; rr < r1 - r0; ++rr) ss += sq[threadIdx.x * PR + rr];
-        s_rstd[threadIdx.x] = ss;      // (its 1/rms values, if any, are no longer needed)
+        cluster.map_shared_rank(s_push, 0)[sp * B + threadIdx.x] = ss;
       }
     }
   }
-  cluster.sync();   // peers may still be reading this CTA's partial until here
-  if (norm_out && a.epi != EPI_SILU) {
-    // CTA 0 of the tile adds the slices' sums in split order: one partial per tile
-    if (sp == 0 && threadIdx.x < B) {
-      float ss = 0.f;
-      for (int q = 0; q < S; ++q) ss += cluster.map_shared_rank(s_rstd, q)[threadIdx.x];
-      a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
-    }
-    cluster.sync();   // peers stay until CTA 0 has read their sums
+  cluster.sync();   // peers' partials are read and the pushed sums have landed in rank 0
+  if (norm_out && a.epi != EPI_SILU && sp == 0 && threadIdx.x < B) {
+    float ss = 0.f;   // one partial per tile: the slices added in split order
+    for (int q = 0; q < S; ++q) ss += s_push[q * B + threadIdx.x];
+    a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
   }
   if (!ok && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
 }
