@@ -67,6 +67,9 @@ def lib():
         L.ora_text_head.argtypes = [P, P, P, P]
         L.ora_depformer.argtypes = [P, P, P, P, P, P, P, P]
         L.ora_step.argtypes = [P] * 10
+        L.ora_rvq_dequantize.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                         ctypes.c_int, ctypes.c_int, P, P]
+        L.ora_rvq_dequantize.restype = None
         _lib = L
     return _lib
 
@@ -220,6 +223,21 @@ class Oracle:
                        lt.ctypes.data if want_logits else None,
                        la.ctypes.data if want_logits else None)
         return col, lt, la
+
+
+def rvq_dequantize(codes, codebooks, code_stride=None):
+    """codes int32 [n, >= n_books] (row f's codes at f*code_stride), codebooks float32
+    [n_books, card, dim] -> (latent float64 [n, dim], count of codes >= card)."""
+    codes = np.ascontiguousarray(codes, dtype=np.int32)
+    cb = np.ascontiguousarray(codebooks, dtype=np.float32)
+    n_books, card, dim = cb.shape
+    n = codes.shape[0]
+    stride = codes.shape[1] if code_stride is None else code_stride
+    out = np.empty((n, dim), dtype=np.float64)
+    bad = ctypes.c_int(0)
+    lib().ora_rvq_dequantize(codes.ctypes.data, stride, n, n_books, cb.ctypes.data, card, dim,
+                             out.ctypes.data, ctypes.byref(bad))
+    return out, bad.value
 
 
 def initial_column(shape):

@@ -310,3 +310,25 @@ void ora_step(const ora_shape* s, const ora_weights* w, ora_session* sess,
   free(z);
   free(lt);
 }
+
+/* ---- Mimi RVQ dequantisation --------------------------------------------------------- */
+
+void ora_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int n_books,
+                        const float* codebooks, int card, int dim, double* out, int* bad) {
+  int nbad = 0;
+  for (int f = 0; f < n_frames; ++f) {
+    double* o = out + (size_t)f * dim;
+    for (int d = 0; d < dim; ++d) o[d] = 0.0;
+    for (int k = 0; k < n_books; ++k) {
+      const int32_t c = codes[(size_t)f * code_stride + k];
+      if (c < 0) continue;
+      if (c >= card) {
+        ++nbad;
+        continue;
+      }
+      const float* e = codebooks + ((size_t)k * card + c) * dim;
+      for (int d = 0; d < dim; ++d) o[d] += (double)e[d];
+    }
+  }
+  if (bad) *bad = nbad;
+}

@@ -107,6 +107,16 @@ void ora_depformer(const ora_shape* s, const ora_weights* w, const double* z,
                    const int32_t* user_codes, int32_t* column, float* logits);
 /* One full tick: embed -> temporal -> text head (greedy or forced) -> depformer ->
  * pos += 1.  logits_text [Vt] and logits_audio [n_q, Va] may be NULL. */
+/* Mimi RVQ dequantisation, the first step after the tick (mhpq section 2.3 "Mimi": 8
+ * codebooks of 2048 entries at 12.5 Hz, residual vector quantisation; Recipe,
+ * Architecture: each output column carries the agent's 8 audio codes).  A residual
+ * quantiser's latent is the sum of the entries it selected, one per codebook:
+ *   out[f][d] = sum_{k < n_books} codebooks[k][codes[f*code_stride + k]][d]
+ * in fp64.  A negative code (the -1 a closed slot emits) adds nothing; a code >= card
+ * adds nothing and is counted in *bad. */
+void ora_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int n_books,
+                        const float* codebooks, int card, int dim, double* out, int* bad);
+
 void ora_step(const ora_shape* s, const ora_weights* w, ora_session* sess,
               const int32_t* prev_column, const int32_t* user_codes,
               const uint8_t* force_mask, const int32_t* forced, int32_t* column,

@@ -49,14 +49,36 @@ def test_ring_attention_matches_oracle(D, W):
             assert np.max(np.abs(got[s, h] - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
 
 
-def test_ring_attention_full_size_sampled():
-    """B=64 slots x 32 heads x 128 over full 3000-position rings; sampled (slot, head)
-    pairs against the oracle."""
+def _check_all(q, k, v, got, n_valid, W):
+    for s in range(got.shape[0]):
+        n = min(n_valid[s], W)
+        for h in range(got.shape[1]):
+            if n <= 0:
+                assert np.all(got[s, h] == 0), (s, h)
+                continue
+            ref = oracle.attend(q[s, h], k[s, h], v[s, h], n)
+            err = np.max(np.abs(got[s, h] - ref))
+            assert err <= TOL * max(1.0, np.max(np.abs(ref))), (s, h, n, err)
+
+
+def test_ring_attention_full_size():
+    """B=64 slots x 32 heads x 128 over full 3000-position rings (the bench workload's
+    attention): every (slot, head) against the oracle."""
     B, H, D, W = 64, 32, 128, 3000
-    q, k, v, got = _run(B, H, D, W, [W] * B, 11)
-    for s, h in [(0, 0), (17, 5), (63, 31)]:
-        ref = oracle.attend(q[s, h], k[s, h], v[s, h], W)
-        assert np.max(np.abs(got[s, h] - ref)) <= TOL * max(1.0, np.max(np.abs(ref)))
+    n_valid = [W] * B
+    q, k, v, got = _run(B, H, D, W, n_valid, 11)
+    _check_all(q, k, v, got, n_valid, W)
+
+
+def test_ring_attention_full_size_ragged():
+    """B=64 at W=3000 with a seeded mix of valid lengths: ragged last chunks, one-key
+    and closed slots, lengths on and next to chunk edges, and lengths above W."""
+    B, H, D, W = 64, 32, 128, 3000
+    edges = [0, 1, 2, 127, 128, 129, 255, 256, 2943, 2944, 2945, 2999, 3000, 3001, 9000]
+    rnd = synth.uniform_i32(B - len(edges), 19, 1, 1, W + 1).tolist()
+    n_valid = edges + rnd
+    q, k, v, got = _run(B, H, D, W, n_valid, 23)
+    _check_all(q, k, v, got, n_valid, W)
 
 
 def test_ring_attention_clamps_valid_lengths():

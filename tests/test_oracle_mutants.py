@@ -32,6 +32,11 @@ MUTANTS = {
     "dep_no_reset_causal": ("for (int j = 0; j <= k; ++j) {\n          const double* kj",
                             "for (int j = 0; j <= k && j < 1; ++j) {\n          const double* kj"),
     "argmax_last_tie": ("if (best < 0 || v[i] > v[best]) best = i;", "if (best < 0 || v[i] >= v[best]) best = i;"),
+    "rvq_wrong_book": ("const float* e = codebooks + ((size_t)k * card + c) * dim;",
+                       "const float* e = codebooks + ((size_t)(k ? k - 1 : 0) * card + c) * dim;"),
+    "rvq_skips_first_book": ("for (int k = 0; k < n_books; ++k) {\n      const int32_t c",
+                             "for (int k = 1; k < n_books; ++k) {\n      const int32_t c"),
+    "rvq_negative_counted": ("      if (c < 0) continue;\n", "      if (c < 0) {\n        ++nbad;\n        continue;\n      }\n"),
 }
 
 

@@ -435,3 +435,68 @@ def test_depformer_inproj_and_step_attention():
         ref = _norm(y, w["dep_out_alpha"], s.eps)
         assert np.allclose(logits[k, :dd], ref, rtol=2e-6, atol=1e-7), k
         assert np.all(logits[k, dd:] == 0)
+
+
+# ---- Mimi RVQ dequantisation -----------------------------------------------------------
+
+def _rvq_books(n_books=8, card=64, dim=16, seed=3):
+    return np.random.default_rng(seed).standard_normal((n_books, card, dim)).astype(np.float32)
+
+
+def test_rvq_single_codebook_returns_its_entry():
+    """With every other code negative (no frame), the latent is exactly the one selected
+    codebook entry."""
+    cb = _rvq_books()
+    for k in range(cb.shape[0]):
+        codes = np.full((1, cb.shape[0]), -1, np.int32)
+        codes[0, k] = 17
+        out, bad = oracle.rvq_dequantize(codes, cb)
+        assert bad == 0
+        assert np.array_equal(out[0], cb[k, 17].astype(np.float64))
+
+
+def test_rvq_is_additive_over_codebooks():
+    """Dequantising codebooks {0..3} and {4..7} separately and adding gives the whole."""
+    cb = _rvq_books()
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, cb.shape[1], size=(20, cb.shape[0]), dtype=np.int32)
+    a, b = codes.copy(), codes.copy()
+    a[:, 4:] = -1
+    b[:, :4] = -1
+    whole, _ = oracle.rvq_dequantize(codes, cb)
+    pa, _ = oracle.rvq_dequantize(a, cb)
+    pb, _ = oracle.rvq_dequantize(b, cb)
+    assert np.allclose(whole, pa + pb, rtol=0, atol=1e-12)
+
+
+def test_rvq_inverts_a_residual_encoder():
+    """A greedy residual quantiser (each stage picks the entry nearest to what the
+    previous stages left) encodes x; dequantising its codes gives x minus the final
+    residual."""
+    cb = _rvq_books(card=256, dim=8)
+    x = np.random.default_rng(9).standard_normal((12, 8))
+    codes = np.empty((12, cb.shape[0]), np.int32)
+    r = x.copy()
+    for k in range(cb.shape[0]):
+        book = cb[k].astype(np.float64)
+        d = ((r[:, None, :] - book[None, :, :]) ** 2).sum(-1)
+        codes[:, k] = d.argmin(1)
+        r = r - book[codes[:, k]]
+    out, bad = oracle.rvq_dequantize(codes, cb)
+    assert bad == 0
+    assert np.allclose(out + r, x, rtol=0, atol=1e-12)
+    assert np.linalg.norm(r) < np.linalg.norm(x)   # the stages did reduce the residual
+
+
+def test_rvq_code_range():
+    """Codes past the codebook add nothing and are counted; negative codes (a closed
+    slot's -1 row) add nothing and are not."""
+    cb = _rvq_books()
+    col = np.random.default_rng(2).integers(0, cb.shape[1], size=(6, 17), dtype=np.int32)
+    col[3, 1] = cb.shape[1]          # one code past the codebook
+    col[4, 1:9] = -1                 # a closed slot's sentinel row
+    out, bad = oracle.rvq_dequantize(col[:, 1:9], cb)
+    assert bad == 1
+    assert np.all(out[4] == 0)
+    ref3 = sum(cb[k, col[3, 1 + k]].astype(np.float64) for k in range(1, 8))
+    assert np.allclose(out[3], ref3, rtol=0, atol=1e-12)
