@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="full", choices=["tiny", "small", "full"])
     ap.add_argument("--engine-flags", type=int, default=0, help="pp_config.flags (PP_FLAG_*)")
+    ap.add_argument("--rvq-iters", type=int, default=50,
+                    help="timed calls of the Mimi RVQ dequantisation (0 = skip that line)")
     ap.add_argument("--skip-user-steps-steps", type=int, default=50,
                     help="ticks of the secondary measurement with PP_FLAG_SKIP_USER_STEPS "
                          "(0 = skip it)")
@@ -284,6 +286,40 @@ def time_ticks(eng, B, shape, steps, warmup, seed_stream):
     return evs[0].elapsed_time(evs[-1]), per
 
 
+def rvq_line(pp, B, iters):
+    """pp_rvq_dequantize timed with CUDA events: once on a [B][17] tick column (the
+    per-tick use: 8 codebooks of 2048 x 512 fp32) and once on a 65536-frame batch.  The
+    32 MB of codebooks stay in L2, so the batch figure is an L2-bound throughput."""
+    import torch
+    import synth
+    n_books, card, dim = 8, 2048, 512
+    cb = torch.from_numpy(synth.normal_f32(n_books * card * dim, SEED, 31, 1.0)).cuda()
+    res = {}
+    for name, n in (("tick_column", B), ("batch_65536", 65536)):
+        stride = 17 if name == "tick_column" else n_books
+        codes = torch.from_numpy(synth.uniform_i32(n * stride, SEED, 32, 0, card)).cuda()
+        ptr = codes.data_ptr() + (4 if stride == 17 else 0)
+        out = torch.empty((n, dim), dtype=torch.float32, device="cuda")
+        s = torch.cuda.current_stream()
+        call = lambda: pp.pp_rvq_dequantize(ptr, stride, n, n_books, cb.data_ptr(), card, dim,
+                                            out.data_ptr(), None, s.cuda_stream)
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(iters):
+            call()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        nbytes = n * (n_books * dim * 4 + dim * 4 + n_books * 4)   # entries read + latent + codes
+        res[name] = {"frames": n, "us_per_call": ms * 1e3, "frames_per_s": n / (ms / 1e3),
+                     "GBps": nbytes / (ms / 1e3) / 1e9}
+    res["note"] = ("8 codebooks x 2048 x 512 fp32 (32 MB, L2-resident); bytes = selected "
+                   "entries read + latent written + codes")
+    return res
+
+
 def main():
     a = parse()
     if a.impl == "reference":
@@ -404,6 +440,11 @@ def main():
         del e2
         torch.cuda.empty_cache()
 
+    # -- Mimi RVQ dequantisation of the tick's agent codes (the first step after the tick) --
+    rvq = None
+    if a.rvq_iters > 0:
+        rvq = rvq_line(pp, B, a.rvq_iters)
+
     # -- B=1 latency line (full shape, fresh session) ---------------------------------------
     b1 = None
     if a.b1_steps > 0:
@@ -443,6 +484,7 @@ def main():
             "kernels_profile": prof,
             "b1": b1,
             "skip_user_steps": skip,
+            "rvq": rvq,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "cpu_baseline": cpu,

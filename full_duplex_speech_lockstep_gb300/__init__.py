@@ -36,7 +36,7 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_session_open", "pp_session_close", "pp_session_import", "pp_session_pos",
            "pp_ring_block", "pp_step", "pp_step_host", "pp_status", "pp_step_kernel_count",
            "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention",
-           "pp_ring_attention_noalloc"]
+           "pp_ring_attention_noalloc", "pp_rvq_dequantize"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -112,6 +112,8 @@ def lib():
         L.pp_ring_attention.restype = I
         L.pp_ring_attention_noalloc.argtypes = [P, P, P, I64, P, I, I, I, I, P, P]
         L.pp_ring_attention_noalloc.restype = I
+        L.pp_rvq_dequantize.argtypes = [P, I, I, I, P, I, I, P, P, P]
+        L.pp_rvq_dequantize.restype = I
         _lib = L
     return _lib
 
@@ -232,6 +234,13 @@ def pp_ring_attention_noalloc(q, k, v, slot_stride, n_valid, B, H, head_dim, win
     """pp_ring_attention with the library's built-in scratch (no allocation)."""
     return _check("pp_ring_attention_noalloc", lib().pp_ring_attention_noalloc(
         q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, stream))
+
+
+def pp_rvq_dequantize(codes, code_stride, n_frames, n_books, codebooks, card, dim, out, status,
+                      stream):
+    """Latent of each frame = sum of the codebook entries its codes select (device)."""
+    return _check("pp_rvq_dequantize", lib().pp_rvq_dequantize(
+        codes, code_stride, n_frames, n_books, codebooks, card, dim, out, status, stream))
 
 
 # ---- convenience wrapper over torch device memory ---------------------------------------

@@ -275,6 +275,27 @@ int pp_ring_attention_noalloc(const float* q, const uint16_t* k, const uint16_t*
                               int64_t slot_stride, const int32_t* n_valid, int B, int H,
                               int head_dim, int window, float* out, void* stream);
 
+/* ---- Mimi RVQ dequantisation: codes to latent, the first step after the tick ---------
+ * The agent's audio rows of each output column are Mimi codes: residual vector
+ * quantisation with 8 codebooks of 2048 entries at 12.5 Hz (mhpq, section 2.3 "Mimi";
+ * Recipe, Architecture).  The codec decoder starts from their latent, which is the sum
+ * of the selected entries:
+ *   out[f][d] = sum_{k < n_books} codebooks[k][codes[f*code_stride + k]][d]
+ * added in codebook order in fp32.
+ *   codes      int32, device, 4-byte aligned; frame f's codes at codes + f*code_stride.
+ *              For a pp_step output column [B][17], pass codes = column + 1 and
+ *              code_stride = 17: the agent rows 1..8.
+ *   codebooks  f32 [n_books][card][dim], device, 16-byte aligned, caller-owned
+ *   out        f32 [n_frames][dim], device, 16-byte aligned
+ *   status     optional device word (e.g. the engine's); PP_S_INDEX is OR-ed into it
+ *              when a code is >= card
+ * A negative code (the -1 of a closed slot) adds nothing; a code >= card adds nothing.
+ * 1 <= n_books <= 32, code_stride >= n_books, dim a positive multiple of 4; n_frames == 0
+ * does nothing.  Asynchronous on `stream`.  Errors: PP_EINVAL, PP_E_CUDA. */
+int pp_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int n_books,
+                      const float* codebooks, int card, int dim, float* out, uint32_t* status,
+                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif
