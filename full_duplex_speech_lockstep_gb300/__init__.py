@@ -15,6 +15,8 @@ raises.
 import ctypes
 import os
 
+import numpy as np
+
 HERE = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(HERE, "libpp.so")
 
@@ -36,7 +38,9 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_session_open", "pp_session_close", "pp_session_import", "pp_session_pos",
            "pp_ring_block", "pp_step", "pp_step_host", "pp_status", "pp_step_kernel_count",
            "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention",
-           "pp_ring_attention_noalloc", "pp_rvq_dequantize"]
+           "pp_ring_attention_noalloc", "pp_rvq_dequantize", "pp_driver_create",
+           "pp_driver_destroy", "pp_driver_open", "pp_driver_close", "pp_driver_phase",
+           "pp_driver_prepare", "pp_driver_absorb", "pp_driver_tick"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -114,6 +118,22 @@ def lib():
         L.pp_ring_attention_noalloc.restype = I
         L.pp_rvq_dequantize.argtypes = [P, I, I, I, P, I, I, P, P, P]
         L.pp_rvq_dequantize.restype = I
+        L.pp_driver_create.argtypes = [I, I, I, ctypes.POINTER(P)]
+        L.pp_driver_create.restype = I
+        L.pp_driver_destroy.argtypes = [P]
+        L.pp_driver_destroy.restype = None
+        L.pp_driver_open.argtypes = [P, P, ctypes.POINTER(pp_prompt), ctypes.POINTER(I)]
+        L.pp_driver_open.restype = I
+        L.pp_driver_close.argtypes = [P, P, I]
+        L.pp_driver_close.restype = I
+        L.pp_driver_phase.argtypes = [P, I]
+        L.pp_driver_phase.restype = I
+        L.pp_driver_prepare.argtypes = [P, P, P, P, P, P]
+        L.pp_driver_prepare.restype = I
+        L.pp_driver_absorb.argtypes = [P, P, P, P]
+        L.pp_driver_absorb.restype = I
+        L.pp_driver_tick.argtypes = [P, P, P, P, P, P]
+        L.pp_driver_tick.restype = I
         _lib = L
     return _lib
 
@@ -234,6 +254,90 @@ def pp_ring_attention_noalloc(q, k, v, slot_stride, n_valid, B, H, head_dim, win
     """pp_ring_attention with the library's built-in scratch (no allocation)."""
     return _check("pp_ring_attention_noalloc", lib().pp_ring_attention_noalloc(
         q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, stream))
+
+
+PP_DRV_FREE, PP_DRV_VOICE, PP_DRV_SILENCE, PP_DRV_PERSONA, PP_DRV_LIVE = 0, 1, 2, 3, 4
+
+
+class pp_prompt(ctypes.Structure):
+    _fields_ = [("voice_frames", ctypes.c_void_p), ("n_voice", ctypes.c_int),
+                ("persona_tokens", ctypes.c_void_p), ("n_persona", ctypes.c_int),
+                ("silence_frame", ctypes.c_void_p), ("silence_ticks", ctypes.c_int)]
+
+
+class Driver:
+    """The session driver (admission, prefill, acoustic delay) over host numpy buffers.
+    With an Engine, tick() runs pp_step through it; without one, prepare()/absorb() give
+    the bookkeeping alone."""
+
+    def __init__(self, max_batch, text_vocab, audio_card):
+        h = ctypes.c_void_p()
+        _check("pp_driver_create", lib().pp_driver_create(max_batch, text_vocab, audio_card,
+                                                          ctypes.byref(h)))
+        self.h, self.B = h, max_batch
+
+    def close_driver(self):
+        if self.h:
+            lib().pp_driver_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close_driver()
+        except Exception:
+            pass
+
+    def open(self, voice=None, persona=None, silence=None, silence_ticks=0, engine=None):
+        keep = []
+        def arr(a):
+            if a is None:
+                return None, 0
+            a = np.ascontiguousarray(a, dtype=np.int32)
+            keep.append(a)
+            return a.ctypes.data, a.shape[0]
+        v, nv = arr(voice)
+        p_, np_ = arr(persona)
+        s_, _ = arr(silence)
+        pr = pp_prompt(v, nv, p_, np_, s_, silence_ticks)
+        slot = ctypes.c_int(-1)
+        _check("pp_driver_open", lib().pp_driver_open(self.h, engine.h if engine else None,
+                                                      ctypes.byref(pr), ctypes.byref(slot)))
+        return slot.value
+
+    def close(self, slot, engine=None):
+        return _check("pp_driver_close",
+                      lib().pp_driver_close(self.h, engine.h if engine else None, slot))
+
+    def phase(self, slot):
+        return lib().pp_driver_phase(self.h, slot)
+
+    def prepare(self, user_frames):
+        u = np.ascontiguousarray(user_frames, dtype=np.int32)
+        prev = np.empty((self.B, 17), np.int32)
+        user = np.empty((self.B, 8), np.int32)
+        mask = np.empty((self.B, 17), np.uint8)
+        forced = np.empty((self.B, 17), np.int32)
+        _check("pp_driver_prepare", lib().pp_driver_prepare(
+            self.h, u.ctypes.data, prev.ctypes.data, user.ctypes.data, mask.ctypes.data,
+            forced.ctypes.data))
+        return prev, user, mask, forced
+
+    def absorb(self, user_frames, column):
+        u = np.ascontiguousarray(user_frames, dtype=np.int32)
+        c = np.ascontiguousarray(column, dtype=np.int32)
+        out = np.empty((self.B, 9), np.int32)
+        _check("pp_driver_absorb", lib().pp_driver_absorb(self.h, u.ctypes.data, c.ctypes.data,
+                                                          out.ctypes.data))
+        return out
+
+    def tick(self, engine, user_frames):
+        u = np.ascontiguousarray(user_frames, dtype=np.int32)
+        out = np.empty((self.B, 9), np.int32)
+        col = np.empty((self.B, 17), np.int32)
+        _check("pp_driver_tick", lib().pp_driver_tick(self.h, engine.h, u.ctypes.data,
+                                                      out.ctypes.data, col.ctypes.data,
+                                                      engine._stream()))
+        return out, col
 
 
 def pp_rvq_dequantize(codes, code_stride, n_frames, n_books, codebooks, card, dim, out, status,

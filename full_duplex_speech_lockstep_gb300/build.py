@@ -1,6 +1,6 @@
 """Build ``libpp.so`` (the tick's kernels + C ABI) in-tree for sm_103a with nvcc.
 
-Each ``csrc/*.cu`` compiles to an object in parallel; the objects link into one shared
+Each ``csrc/*.cu`` (and host-only ``csrc/*.cpp``) compiles to an object in parallel; the objects link into one shared
 library next to this file.  The CUDA runtime is linked statically.
 """
 import concurrent.futures
@@ -19,7 +19,8 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # kernels (.cu) and host-only runtime code (.cpp), both through nvcc
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -34,7 +35,7 @@ def stale():
 
 
 def _compile(src, log):
-    obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+    obj = os.path.join(OBJ, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [NVCC] + ARCH + FLAGS + ["-I", INCLUDE, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     log.append((src, r.stdout + r.stderr))

@@ -275,6 +275,68 @@ int pp_ring_attention_noalloc(const float* q, const uint16_t* k, const uint16_t*
                               int64_t slot_stride, const int32_t* n_valid, int B, int H,
                               int head_dim, int window, float* out, void* stream);
 
+/* ---- session driver: host bookkeeping around pp_step ------------------------------
+ * Admission and recycle of slots, the persona / voice prefill and the acoustic delay,
+ * all on the host (no device memory).  Sessions exchange ALIGNED frames with the
+ * driver: one frame = the 8 codes of one 80 ms Mimi frame (and, for the agent, its text
+ * token).  In the model's columns the acoustic codebooks 1..7 of each stream run one
+ * frame behind codebook 0 and the text (mhpq 3.3, "80 ms frame + 80 ms acoustic
+ * delay"), so the driver feeds the user rows of tick t as [U_t[0], U_{t-1}[1..7]] and
+ * returns agent frame f = (text and codebook 0 of tick f, codebooks 1..7 of tick f+1),
+ * one tick late.  The initial token (audio_card) stands in for frame -1.
+ * Prefill (mhpq, "Persona Voice 注入": voice + 2 x silence + persona): n_voice ticks of
+ * voice-prompt frames, silence_ticks of silence, n_persona ticks with the text row
+ * forced to the persona tokens (audio silent), silence_ticks of silence, then live.
+ * Forced agent frames are shifted exactly like generated ones. */
+typedef struct pp_driver pp_driver;
+
+typedef struct {
+  const int32_t* voice_frames;    /* [n_voice][8] aligned voice-prompt codes, host (copied) */
+  int n_voice;
+  const int32_t* persona_tokens;  /* [n_persona] text tokens, host (copied) */
+  int n_persona;
+  const int32_t* silence_frame;   /* [8] aligned codes of one silence frame, host (copied);
+                                     NULL: the initial token in every codebook */
+  int silence_ticks;              /* length of each of the two silence stretches */
+} pp_prompt;
+
+enum { PP_DRV_FREE = 0, PP_DRV_VOICE = 1, PP_DRV_SILENCE = 2, PP_DRV_PERSONA = 3,
+       PP_DRV_LIVE = 4 };
+
+/* A driver for an engine of max_batch slots.  Errors: PP_EINVAL. */
+int pp_driver_create(int max_batch, int text_vocab, int audio_card, pp_driver** out);
+void pp_driver_destroy(pp_driver* d);
+
+/* Admit a session into the lowest free slot (*slot), also opening it on `e` when e is
+ * not NULL.  Codes must lie in [0, audio_card], text tokens in [0, text_vocab].
+ * Errors: PP_EINVAL, PP_E_BUSY (no free slot), or pp_session_open's error. */
+int pp_driver_open(pp_driver* d, pp_engine* e, const pp_prompt* prompt, int* slot);
+
+/* End the session in `slot` (and close it on `e` when not NULL); the slot is free for
+ * the next admission.  Errors: PP_EINVAL, PP_E_RANGE, PP_E_NOTLIVE. */
+int pp_driver_close(pp_driver* d, pp_engine* e, int slot);
+
+/* Phase of the slot's next tick (PP_DRV_*), or PP_EINVAL / PP_E_RANGE. */
+int pp_driver_phase(const pp_driver* d, int slot);
+
+/* Inputs of the next pp_step from this tick's aligned user frames [max_batch][8]: all
+ * host buffers of pp_step's layouts.  Does not change the driver.  Errors: PP_EINVAL
+ * (NULL buffer, or a user code outside [0, audio_card] in an open slot). */
+int pp_driver_prepare(pp_driver* d, const int32_t* user_frames, int32_t* prev_column,
+                      int32_t* user_codes, uint8_t* force_mask, int32_t* forced);
+
+/* Take the tick's output column [max_batch][17] (host) and the same user frames;
+ * writes agent_frames [max_batch][9] (text + 8 codes): the frame this tick completed,
+ * or -1 in every entry when none (a closed slot, or a session's first tick).  Advances
+ * every open slot by one tick.  Errors: PP_EINVAL. */
+int pp_driver_absorb(pp_driver* d, const int32_t* user_frames, const int32_t* column,
+                     int32_t* agent_frames);
+
+/* prepare + pp_step_host + absorb on engine `e`; column_out [max_batch][17] may be
+ * NULL.  Blocks until the tick's results are on the host.  Errors: as the three. */
+int pp_driver_tick(pp_driver* d, pp_engine* e, const int32_t* user_frames,
+                   int32_t* agent_frames, int32_t* column_out, void* stream);
+
 /* ---- Mimi RVQ dequantisation: codes to latent, the first step after the tick ---------
  * The agent's audio rows of each output column are Mimi codes: residual vector
  * quantisation with 8 codebooks of 2048 entries at 12.5 Hz (mhpq, section 2.3 "Mimi";
