@@ -69,9 +69,9 @@ struct Cfg {
   static constexpr int kStages = (96 * 1024) / kStageBytes < 8 ? (96 * 1024) / kStageBytes : 8;
   static constexpr int kTmemCols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, 1/rms*/;
-  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][129] floats, then
+  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][132] floats, then
   // the pushed slice sums [kMaxSplits][64] floats at 72 KB
-  static_assert(2 * (N / 2) * 129 * 4 <= 72 * 1024, "epilogue partials overlap the push area");
+  static_assert(2 * (N / 2) * 132 * 4 <= 72 * 1024, "epilogue partials overlap the push area");
   static_assert(72 * 1024 + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
 };
 
@@ -314,14 +314,12 @@ __global__ void __launch_bounds__(128, 2)
   }
 
   // ---- split-K across the thread-block cluster (one CTA per split of this tile) ----------
-  // Each CTA parks its partial [128 rows][B] in its own shared memory; after a cluster
-  // barrier, CTA `sp` reduces a slice of the tile's rows by reading the S partials
-  // through distributed shared memory in split order 0..S-1, and applies the epilogue.
-  // Every CTA passes both cluster barriers, also after a timeout.
-  // The partial is parked slot-major, [slot][row] with a padded row count, so that the
-  // reducing threads (rows fastest) read contiguous runs of peer memory and write
-  // contiguous rows of y and of the next operand.
-  constexpr int PR = 129;
+  // Each CTA parks its partial [slot][row] (row stride PR) in its own shared memory;
+  // after a cluster barrier, CTA `sp` reduces a slice of the tile's rows, 4 rows aligned
+  // to 4 per thread and step, reading the S partials through distributed shared memory
+  // with 16-byte loads and adding them in split order 0..S-1; then it applies the
+  // epilogue.  Every CTA passes both cluster barriers, also after a timeout.
+  constexpr int PR = 132;                    // row stride of a parked partial (16 bytes)
   float* mine = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int b = 0; b < N / 2; ++b)
@@ -334,82 +332,145 @@ __global__ void __launch_bounds__(128, 2)
   const float* peer[kMaxSplits];
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? cluster.map_shared_rank(mine, q) : mine;
+  auto ld4 = [](const float* p) { return *reinterpret_cast<const float4*>(p); };
+  constexpr int CH = 2;   // 4-row units per thread and step: up to 2*S 16-byte peer loads
   if (a.epi == EPI_SILU) {
-    const int p0 = (sp * 64) / S, p1 = ((sp + 1) * 64) / S;
-    const int n = (p1 - p0) * B;
-    const int prs = p1 - p0;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const int p = p0 + e % prs, b = e / prs;
-      float gv[kMaxSplits], uv[kMaxSplits];
-#pragma unroll
-      for (int q = 0; q < kMaxSplits; ++q)
-        if (q < S) {
-          gv[q] = peer[q][b * PR + p];
-          uv[q] = peer[q][b * PR + p + 64];
-        }
-      float g = 0.f, u = 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxSplits; ++q)
-        if (q < S) { g += gv[q]; u += uv[q]; }
-      if (norm_in) { g *= s_rstd[b]; u *= s_rstd[b]; }
-      const int mm = mt * 64 + p;
-      if (mm < a.pair_rows) op_store(a.op_out, a.ld_op, a.Bp_out, b, mm, g / (1.0f + expf(-g)) * u);
-    }
-  } else {
-    // this CTA's slice of rows, processed 8 elements per pass so that up to 8*S
-    // distributed-shared-memory loads (and the residual loads) are in flight at once
-    const int r0 = (sp * 128) / S, r1 = ((sp + 1) * 128) / S;
-    const int n = (r1 - r0) * B;
-    constexpr int CH = 8;
-    float* sq = mine + (N / 2) * PR;  // [slot][row - r0] y^2 of this slice (fused RMSNorm)
-    const int rows = r1 - r0;
-    for (int e0 = threadIdx.x; e0 < n; e0 += CH * (int)blockDim.x) {
-      int off[CH], mrow[CH], bcol[CH];
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {   // rows fastest across threads: coalesced y / operand
-        const int e = e0 + i * (int)blockDim.x;
-        const int rr = r0 + e % rows;
-        bcol[i] = e / rows;
-        mrow[i] = (e < n) ? mt * 128 + rr : a.M;     // a.M marks "no element"
-        off[i] = bcol[i] * PR + rr;
-      }
-      float ex[CH], al[CH];   // residual (or embedding) and norm gain, loaded with the partials
+    // slice of the 64 gate/up pairs in whole 4-pair groups; unit = (slot, 4 pairs)
+    const int p0 = 4 * ((sp * 16) / S), p1 = 4 * (((sp + 1) * 16) / S);
+    const int G = (p1 - p0) / 4;
+    const int n = G * B;
+    for (int u0 = threadIdx.x; u0 < n; u0 += CH * (int)blockDim.x) {
+      int off[CH], mm[CH], bc[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        ex[i] = (a.epi != EPI_STORE && mrow[i] < a.M) ? epi_extra(a, bcol[i], mrow[i]) : 0.f;
-        al[i] = (norm_out && mrow[i] < a.M) ? a.norm_alpha[mrow[i]] : 0.f;
+        const int u = u0 + i * (int)blockDim.x;
+        const int g = u % G;
+        bc[i] = u / G;
+        mm[i] = (u < n) ? mt * 64 + p0 + 4 * g : a.pair_rows;   // pair_rows: no unit
+        off[i] = bc[i] * PR + p0 + 4 * g;
       }
-      float pv[CH][kMaxSplits];
+      float4 gv[CH][kMaxSplits], uv[CH][kMaxSplits];
 #pragma unroll
       for (int i = 0; i < CH; ++i)
 #pragma unroll
         for (int q = 0; q < kMaxSplits; ++q)
-          if (q < S && mrow[i] < a.M) pv[i][q] = peer[q][off[i]];
+          if (q < S && mm[i] < a.pair_rows) {
+            gv[i][q] = ld4(peer[q] + off[i]);
+            uv[i][q] = ld4(peer[q] + off[i] + 64);
+          }
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        const int e = e0 + i * (int)blockDim.x;
-        if (mrow[i] < a.M) {
-          float v = 0.f;
+        if (mm[i] >= a.pair_rows) continue;
+        float g4[4] = {0.f, 0.f, 0.f, 0.f}, u4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int q = 0; q < kMaxSplits; ++q)
-            if (q < S) v += pv[i][q];
-          if (norm_in) v *= s_rstd[bcol[i]];
-          const float y = v + ex[i];
-          a.Y[(size_t)bcol[i] * a.ldy + mrow[i]] = y;
-          if (norm_out) {
-            op_store(a.norm_op, a.M, Bp, bcol[i], mrow[i], al[i] * y);
-            sq[off[i] - r0] = y * y;
+        for (int q = 0; q < kMaxSplits; ++q)
+          if (q < S) {
+            g4[0] += gv[i][q].x; g4[1] += gv[i][q].y; g4[2] += gv[i][q].z; g4[3] += gv[i][q].w;
+            u4[0] += uv[i][q].x; u4[1] += uv[i][q].y; u4[2] += uv[i][q].z; u4[3] += uv[i][q].w;
           }
-        } else if (norm_out && e < n) {
-          sq[off[i] - r0] = 0.f;     // rows past the matrix add nothing
+        const float rs = norm_in ? s_rstd[bc[i]] : 1.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (mm[i] + c >= a.pair_rows) break;
+          float g = g4[c], u = u4[c];
+          if (norm_in) { g *= rs; u *= rs; }
+          op_store(a.op_out, a.ld_op, a.Bp_out, bc[i], mm[i] + c, g / (1.0f + expf(-g)) * u);
         }
+      }
+    }
+  } else {
+    // slice of the tile's 128 rows in whole 4-row groups; unit = (slot, 4 rows); units
+    // run rows fastest across threads, so y and the next operand are written in rows
+    const int r0 = 4 * ((sp * 32) / S), r1 = 4 * (((sp + 1) * 32) / S);
+    const int G = (r1 - r0) / 4;
+    const int n = G * B;
+    float* sq = mine + (N / 2) * PR;  // [slot][row - r0] y^2 of this slice (fused RMSNorm)
+    for (int u0 = threadIdx.x; u0 < n; u0 += CH * (int)blockDim.x) {
+      int off[CH], mrow[CH], bcol[CH];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int u = u0 + i * (int)blockDim.x;
+        const int g = u % G;
+        bcol[i] = u / G;
+        mrow[i] = (u < n) ? mt * 128 + r0 + 4 * g : a.M;   // a.M marks "no unit"
+        off[i] = bcol[i] * PR + r0 + 4 * g;
+      }
+      float4 ex[CH], al[CH];   // residual (or embedding) and norm gains of the 4 rows
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        ex[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        al[i] = ex[i];
+        if (mrow[i] < a.M) {
+          if (a.epi == EPI_ADD) {
+            ex[i] = ld4(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]);
+          } else if (a.epi == EPI_EMB) {
+            const uint2 w = *reinterpret_cast<const uint2*>(
+                a.emb + (size_t)a.tok[bcol[i]] * a.M + mrow[i]);
+            ex[i] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                                __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+          }
+          if (norm_out) al[i] = ld4(a.norm_alpha + mrow[i]);
+        }
+      }
+      float4 pv[CH][kMaxSplits];
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q)
+          if (q < S && mrow[i] < a.M) pv[i][q] = ld4(peer[q] + off[i]);
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        if (mrow[i] >= a.M) continue;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q)
+          if (q < S) {
+            v[0] += pv[i][q].x; v[1] += pv[i][q].y; v[2] += pv[i][q].z; v[3] += pv[i][q].w;
+          }
+        const float rs = norm_in ? s_rstd[bcol[i]] : 1.f;
+        const float exv[4] = {ex[i].x, ex[i].y, ex[i].z, ex[i].w};
+        const float alv[4] = {al[i].x, al[i].y, al[i].z, al[i].w};
+        float y[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float vv = v[c];
+          if (norm_in) vv *= rs;
+          y[c] = vv + exv[c];
+        }
+        *reinterpret_cast<float4*>(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]) =
+            make_float4(y[0], y[1], y[2], y[3]);
+        if (norm_out) {
+          uint16_t hi[4], lo[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) bf16_split(alv[c] * y[c], hi[c], lo[c]);
+          *reinterpret_cast<uint2*>(a.norm_op + (size_t)bcol[i] * a.M + mrow[i]) =
+              make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16),
+                         (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+          *reinterpret_cast<uint2*>(a.norm_op + (size_t)(Bp + bcol[i]) * a.M + mrow[i]) =
+              make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16),
+                         (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+          *reinterpret_cast<float4*>(sq + off[i] - r0) =
+              make_float4(y[0] * y[0], y[1] * y[1], y[2] * y[2], y[3] * y[3]);
+        }
+      }
+      if (norm_out) {   // units past the matrix rows add nothing
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+          if (mrow[i] >= a.M && u0 + i * (int)blockDim.x < n)
+            *reinterpret_cast<float4*>(sq + off[i] - r0) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     if (norm_out) {   // this slice's sums of y^2, in row order, pushed to rank 0 of the tile
       __syncthreads();
       if (threadIdx.x < B) {
         float ss = 0.f;
-        for (int rr = 0; rr < r1 - r0; ++rr) ss += sq[threadIdx.x * PR + rr];
+        for (int rr = 0; rr < r1 - r0; rr += 4) {
+          const float4 w = ld4(sq + threadIdx.x * PR + rr);
+          ss += w.x;
+          ss += w.y;
+          ss += w.z;
+          ss += w.w;
+        }
         cluster.map_shared_rank(s_push, 0)[sp * B + threadIdx.x] = ss;
       }
     }

@@ -312,6 +312,8 @@ bool plan_mm(Mm* g, const void* w, int rows_total, int M, int K, int pair, const
   g->M = M;
   g->K = K;
   g->pair = pair;
+  // the split-K epilogue moves rows in aligned groups of 4
+  if (!pair && M % 4) return false;
   g->kblocks = (K + 63) / 64;
   g->m_tiles = pair ? (pair + 63) / 64 : (M + 127) / 128;
   if (g->m_tiles > kMaxTiles) return false;
