@@ -115,3 +115,56 @@ def test_isolation_across_engine_sizes():
         user, fm, fo = schedules.prefill_session(s, 100 + i, T=20, voice=3, persona=4)
         sess.append((i, i % 5, user, fm, fo))
     _check_isolation(s, 64, sess[:1] + sess[1:], 25, device_weights(w))
+
+
+def test_isolation_full_shape_attention_merge_paths():
+    """Full shape (2 layers), every ring full at position 3000: slots of a 64-slot engine
+    against the same sessions alone.  At B=64 most (slot, head) pairs of the tensor-core
+    attention are merged on chip; alone, every pair is split across CTAs and merged
+    through global partials.  Columns and logits must be bit-identical."""
+    import dataclasses
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    shape = dataclasses.replace(synth.FULL, n_layers=2)
+    W, seed, T = shape.window, 29, 3
+    w_dev = synth.make_weights_device(shape, seed)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def fill(eng, slots_src):
+        for dst, src in enumerate(slots_src):
+            for l in range(shape.n_layers):
+                for kv in range(2):
+                    synth.ring_kv_fill_device(eng.ring_block(l, dst, kv), shape, seed, src, l,
+                                              kv, stream)
+            eng.import_session(dst, W)
+        torch.cuda.synchronize()
+
+    def run(eng, B, slots_src):
+        ld = shape.text_vocab + shape.n_q * shape.audio_card
+        logits = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+        prev = torch.from_numpy(np.tile(initial_column(shape), (B, 1))).cuda()
+        cols, lgs = [], []
+        for t in range(T):
+            user = np.stack([synth.uniform_i32(8, seed, 300 + t * 64 + s, 0, shape.audio_card)
+                             for s in slots_src])
+            col = eng.step(prev, torch.from_numpy(user).cuda(), logits=logits)
+            cols.append(col.cpu().numpy().copy())
+            lgs.append(logits.cpu().numpy().copy())
+            prev = col.clone()
+        return np.stack(cols), np.stack(lgs)
+
+    B = 64
+    eng = pp.Engine(shape, B, w_dev, flags=EXTRA_FLAGS)
+    fill(eng, list(range(B)))
+    bc, bl = run(eng, B, list(range(B)))
+    assert eng.status() == 0
+    eng.close_engine()
+    del eng
+    torch.cuda.empty_cache()
+    for s in (0, 37, 63):
+        e1 = pp.Engine(shape, 1, w_dev, flags=EXTRA_FLAGS)
+        fill(e1, [s])
+        ac, al = run(e1, 1, [s])
+        e1.close_engine()
+        assert np.array_equal(bc[:, s], ac[:, 0]), ("columns differ", s)
+        assert np.array_equal(bl[:, s].view(np.uint32), al[:, 0].view(np.uint32)), ("logits", s)
