@@ -70,6 +70,14 @@ def lib():
         L.ora_rvq_dequantize.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                          ctypes.c_int, ctypes.c_int, P, P]
         L.ora_rvq_dequantize.restype = None
+        L.ora_philox4x64.argtypes = [P, P, P]
+        L.ora_philox4x64.restype = None
+        L.ora_sample_uniform.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int]
+        L.ora_sample_uniform.restype = ctypes.c_float
+        L.ora_sample.argtypes = [P, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float,
+                                 ctypes.c_float, P, ctypes.c_int, ctypes.c_float,
+                                 ctypes.c_double, P, P]
+        L.ora_sample.restype = ctypes.c_int32
         _lib = L
     return _lib
 
@@ -238,6 +246,38 @@ def rvq_dequantize(codes, codebooks, code_stride=None):
     lib().ora_rvq_dequantize(codes.ctypes.data, stride, n, n_books, cb.ctypes.data, card, dim,
                              out.ctypes.data, ctypes.byref(bad))
     return out, bad.value
+
+
+def philox4x64(counter, key):
+    """Philox4x64-10 block: counter (4 x uint64), key (2 x uint64) -> 4 x uint64."""
+    c = np.ascontiguousarray(counter, dtype=np.uint64)
+    k = np.ascontiguousarray(key, dtype=np.uint64)
+    out = np.empty(4, dtype=np.uint64)
+    lib().ora_philox4x64(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    return out
+
+
+def sample_uniform(seed, pos, row):
+    """The uniform deciding row `row` (0 text, 1..8 agent audio) at session position pos."""
+    return float(lib().ora_sample_uniform(int(seed) & (2**64 - 1), int(pos), int(row)))
+
+
+# relative distance to a decision boundary below which fp32 masses and expf on the GPU
+# may take either side (the masses carry well under 1e-5 relative rounding error)
+SAMPLE_TOL = 1e-4
+
+
+def sample(logits, u, temperature=1.0, top_k=0, top_p=1.0, penalty=1.0, history=(),
+           tol=SAMPLE_TOL):
+    """One sampled token from fp32 logits -> (token, ambiguous, n_kept)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    h = np.ascontiguousarray(np.asarray(history, dtype=np.int32).reshape(-1))
+    amb = ctypes.c_int(0)
+    kept = ctypes.c_int(0)
+    t = lib().ora_sample(lg.ctypes.data, lg.size, float(temperature), int(top_k), float(top_p),
+                         float(penalty), h.ctypes.data if h.size else None, int(h.size),
+                         float(u), float(tol), ctypes.byref(amb), ctypes.byref(kept))
+    return int(t), bool(amb.value), int(kept.value)
 
 
 def initial_column(shape):

@@ -332,3 +332,163 @@ void ora_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int
   }
   if (bad) *bad = nbad;
 }
+
+/* ---- sampling variants ------------------------------------------------------------
+ *
+ * The pages decode greedily and list the knobs a deployment may turn instead:
+ * temperature, nucleus (top-p), repetition penalty and a separate audio temperature
+ * ("PersonaPlex ... vLLM-Omni", deployment config; the persona-tuning article,
+ * "generation parameters" and "repetition penalty").  They define none of the steps,
+ * so the reading below is the plainest one that these knobs support, in this order:
+ *   1. repetition penalty on the raw logits, in the signed form of Keskar et al.
+ *      (CTRL, 2019) as commonly applied: each distinct token of the given history has
+ *      its logit divided by R when positive and multiplied by R otherwise;
+ *   2. division by the temperature;
+ *   3. top-k: keep the logits at or above the k-th largest (ties at it are kept);
+ *   4. e_i = exp(v_i - max v) over the kept logits;
+ *   5. nucleus: the threshold is the largest e value whose own mass plus the mass of
+ *      every larger e reaches p * sum(e); keep e at or above it (ties kept);
+ *   6. inverse CDF in index order: the first kept index whose running mass exceeds
+ *      u * (kept mass), else the last kept index.
+ * Logits that are not finite are never chosen; with nothing left the token is 0.
+ * Steps 1-4 are taken in fp32 (the decision's precision on the GPU: one IEEE
+ * division or product per step, then expf), masses are accumulated in fp64.
+ */
+
+/* Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011): ten rounds of two 64x64->128 multiplications with the published
+ * multipliers, the key bumped by the published Weyl constants between rounds. */
+void ora_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const unsigned __int128 p0 = (unsigned __int128)M0 * c0;
+    const unsigned __int128 p1 = (unsigned __int128)M1 * c2;
+    const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+    const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+    const uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniform that decides row r (0 text, 1..8 agent audio) of the tick at session
+ * position pos: word r % 4 of the Philox block at counter (pos, r / 4, 0, 0) under the
+ * key (seed, 0), its top 24 bits scaled by 2^-24 (exact in fp32, in [0, 1)). */
+float ora_sample_uniform(uint64_t seed, int64_t pos, int row) {
+  const uint64_t ctr[4] = {(uint64_t)pos, (uint64_t)(row / 4), 0, 0};
+  const uint64_t key[2] = {seed, 0};
+  uint64_t out[4];
+  ora_philox4x64(ctr, key, out);
+  return (float)(out[row % 4] >> 40) * (1.0f / 16777216.0f);
+}
+
+static int cmp_f32_desc(const void* a, const void* b) {
+  const float x = *(const float*)a, y = *(const float*)b;
+  return (x < y) - (x > y);
+}
+
+int32_t ora_sample(const float* logits, int n, float temperature, int top_k, float top_p,
+                   float penalty, const int32_t* hist, int n_hist, float u, double tol,
+                   int* ambiguous, int* n_kept) {
+  float* v = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+  float* e = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+  float* srt = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
+  int amb = 0;
+  for (int i = 0; i < n; ++i) v[i] = logits[i];
+  /* 1. repetition penalty, once per distinct history token */
+  for (int j = 0; j < n_hist; ++j) {
+    const int32_t h = hist[j];
+    if (h < 0 || h >= n) continue;
+    int seen = 0;
+    for (int i = 0; i < j; ++i) seen |= (hist[i] == h);
+    if (seen) continue;
+    v[h] = v[h] > 0.f ? v[h] / penalty : v[h] * penalty;
+  }
+  /* 2. temperature */
+  int n_fin = 0;
+  float m = -INFINITY;
+  for (int i = 0; i < n; ++i) {
+    v[i] = v[i] / temperature;
+    if (isfinite(v[i])) {
+      srt[n_fin++] = v[i];
+      if (v[i] > m) m = v[i];
+    }
+  }
+  if (n_fin == 0) {
+    free(v); free(e); free(srt);
+    if (ambiguous) *ambiguous = 0;
+    if (n_kept) *n_kept = 0;
+    return 0;
+  }
+  /* 3. top-k threshold: the k-th largest finite value */
+  float tk = -INFINITY;
+  if (top_k > 0 && top_k < n_fin) {
+    qsort(srt, (size_t)n_fin, sizeof(float), cmp_f32_desc);
+    tk = srt[top_k - 1];
+  }
+  /* 4. exponentials against the maximum */
+  double Z = 0.0;
+  for (int i = 0; i < n; ++i) {
+    e[i] = (isfinite(v[i]) && v[i] >= tk) ? expf(v[i] - m) : 0.f;
+    Z += (double)e[i];
+  }
+  /* 5. nucleus threshold: walk the e values from the largest down, a run of equal
+   * values at a time, until the mass reaches p * Z */
+  float tp = 0.f;
+  if (top_p < 1.f) {
+    int ne = 0;
+    for (int i = 0; i < n; ++i)
+      if (e[i] > 0.f) srt[ne++] = e[i];
+    qsort(srt, (size_t)ne, sizeof(float), cmp_f32_desc);
+    const double P = (double)top_p * Z;
+    double mass = 0.0;
+    int j = 0;
+    while (j < ne) {
+      const int start = j;
+      const float val = srt[j];
+      const double before = mass;
+      while (j < ne && srt[j] == val) mass += (double)srt[j++];
+      if (mass >= P) {
+        tp = val;
+        /* near the cut the GPU's fp32 masses and expf may land on either side */
+        if (mass - P < tol * Z || P - before < tol * Z) amb = 1;
+        if (j < ne && (double)srt[j] >= (double)val * (1.0 - tol)) amb = 1;
+        if (start > 0 && (double)srt[start - 1] <= (double)val * (1.0 + tol)) amb = 1;
+        break;
+      }
+    }
+  }
+  /* 6. inverse CDF in index order over the kept set */
+  double ZK = 0.0;
+  int last = -1, kept = 0;
+  for (int i = 0; i < n; ++i)
+    if (e[i] > 0.f && e[i] >= tp) {
+      ZK += (double)e[i];
+      last = i;
+      ++kept;
+    }
+  const double target = (double)u * ZK;
+  double run = 0.0;
+  int tok = last;
+  for (int i = 0; i < n; ++i) {
+    if (!(e[i] > 0.f && e[i] >= tp)) continue;
+    const double before = run;
+    run += (double)e[i];
+    if (run > target) {
+      tok = i;
+      if (run - target < tol * ZK || target - before < tol * ZK) amb = 1;
+      break;
+    }
+  }
+  free(v); free(e); free(srt);
+  if (ambiguous) *ambiguous = amb;
+  if (n_kept) *n_kept = kept;
+  return tok < 0 ? 0 : tok;
+}

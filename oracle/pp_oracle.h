@@ -117,6 +117,16 @@ void ora_depformer(const ora_shape* s, const ora_weights* w, const double* z,
 void ora_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int n_books,
                         const float* codebooks, int card, int dim, double* out, int* bad);
 
+/* Sampling variants (the reading is stated at the definitions in pp_oracle.c).
+ * ora_sample returns the token; *ambiguous is set when the decision lies within tol
+ * (relative) of a boundary that fp32 masses or expf could move, *n_kept counts the
+ * tokens left after the filters. */
+void ora_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+float ora_sample_uniform(uint64_t seed, int64_t pos, int row);
+int32_t ora_sample(const float* logits, int n, float temperature, int top_k, float top_p,
+                   float penalty, const int32_t* hist, int n_hist, float u, double tol,
+                   int* ambiguous, int* n_kept);
+
 void ora_step(const ora_shape* s, const ora_weights* w, ora_session* sess,
               const int32_t* prev_column, const int32_t* user_codes,
               const uint8_t* force_mask, const int32_t* forced, int32_t* column,

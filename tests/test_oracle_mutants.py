@@ -37,7 +37,25 @@ MUTANTS = {
     "rvq_skips_first_book": ("for (int k = 0; k < n_books; ++k) {\n      const int32_t c",
                              "for (int k = 1; k < n_books; ++k) {\n      const int32_t c"),
     "rvq_negative_counted": ("      if (c < 0) continue;\n", "      if (c < 0) {\n        ++nbad;\n        continue;\n      }\n"),
+    "philox_key_bump_swapped": ("      k0 += W0;\n      k1 += W1;", "      k0 += W1;\n      k1 += W0;"),
+    "philox_products_swapped": ("const uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;",
+                                "const uint64_t n0 = hi0 ^ c1 ^ k0, n1 = lo0, n2 = hi1 ^ c3 ^ k1, n3 = lo1;"),
+    "uniform_low_bits": ("(float)(out[row % 4] >> 40)", "(float)(out[row % 4] & 0xFFFFFFu)"),
+    "uniform_block_by_word": ("(uint64_t)(row / 4), 0, 0}", "(uint64_t)(row % 4), 0, 0}"),
+    "temperature_multiplies": ("v[i] = v[i] / temperature;", "v[i] = v[i] * temperature;"),
+    "penalty_unsigned": ("v[h] = v[h] > 0.f ? v[h] / penalty : v[h] * penalty;", "v[h] = v[h] / penalty;"),
+    "penalty_per_occurrence": ("    if (seen) continue;\n", "    (void)seen;\n"),
+    "top_k_off_by_one": ("tk = srt[top_k - 1];", "tk = srt[top_k];"),
+    "nucleus_drops_the_cut": ("        tp = val;\n", "        tp = start > 0 ? srt[start - 1] : val;\n"),
+    "cdf_not_strict": ("    if (run > target) {", "    if (run >= target) {"),
+    "cdf_ignores_kept_set": ("    if (!(e[i] > 0.f && e[i] >= tp)) continue;\n", "    if (!(e[i] > 0.f)) continue;\n"),
 }
+
+# mistakes in the sampling variants, caught by their own pin file
+SAMPLING = {"philox_key_bump_swapped", "philox_products_swapped", "uniform_low_bits",
+            "uniform_block_by_word", "temperature_multiplies", "penalty_unsigned",
+            "penalty_per_occurrence", "top_k_off_by_one", "nucleus_drops_the_cut",
+            "cdf_not_strict", "cdf_ignores_kept_set"}
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -51,7 +69,8 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
                            "-std=c11", str(tmp_path / "pp_oracle.c"), "-o", so, "-lm"])
     env = dict(os.environ, PP_ORACLE_SO=so)
+    pins = "test_oracle_sampling_pins.py" if name in SAMPLING else "test_oracle_pins.py"
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", pins)],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "planted mistake %s was not caught:\n%s" % (name, r.stdout[-2000:])

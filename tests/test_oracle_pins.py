@@ -500,3 +500,4 @@ def test_rvq_code_range():
     assert np.all(out[4] == 0)
     ref3 = sum(cb[k, col[3, 1 + k]].astype(np.float64) for k in range(1, 8))
     assert np.allclose(out[3], ref3, rtol=0, atol=1e-12)
+
