@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--skip-user-steps-steps", type=int, default=50,
                     help="ticks of the secondary measurement with PP_FLAG_SKIP_USER_STEPS "
                          "(0 = skip it)")
+    ap.add_argument("--sampling-steps", type=int, default=50,
+                    help="ticks of the secondary measurement with every slot sampled "
+                         "(0 = skip it)")
     ap.add_argument("--layers", type=int, default=0,
                     help="temporal layers (0 = the shape's own); fewer layers give a small "
                          "case with full-size kernels for profiling")
@@ -420,6 +423,22 @@ def main():
         dt = time.perf_counter() - t0
         dt = max_over_ranks(ws, dt)
         e2e_val = sum_over_ranks(ws, B * a.e2e_steps) / dt
+    # -- the same engine with every slot sampled (the pages' generation parameters) --------
+    samp = None
+    if a.sampling_steps > 0:
+        params = dict(text_temperature=0.7, text_top_p=0.9, repetition_penalty=1.2,
+                      penalty_window=64, audio_temperature=0.3)
+        for slot in range(B):
+            eng.set_sampling(slot, seed=1000 + slot, **params)
+        ms3, per3 = time_ticks(eng, B, shape, a.sampling_steps, max(3, a.warmup // 4), 900)
+        ms3 = max_over_ranks(ws, ms3)
+        samp = {"value": sum_over_ranks(ws, B * a.sampling_steps) / (ms3 / 1000.0),
+                "unit": UNIT, "ms_per_step": ms3 / a.sampling_steps,
+                "p50_tick_ms": float(np.percentile(per3, 50)), "params": params,
+                "note": "every slot sampled: text temperature + nucleus + repetition penalty, "
+                        "audio temperature"}
+        for slot in range(B):
+            eng.set_sampling(slot)
     status = eng.status()
     eng.close_engine()
     del eng
@@ -484,6 +503,7 @@ def main():
             "kernels_profile": prof,
             "b1": b1,
             "skip_user_steps": skip,
+            "sampling": samp,
             "rvq": rvq,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

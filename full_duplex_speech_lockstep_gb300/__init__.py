@@ -40,7 +40,8 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_profile_step", "pp_ring_attention_scratch_bytes", "pp_ring_attention",
            "pp_ring_attention_noalloc", "pp_rvq_dequantize", "pp_driver_create",
            "pp_driver_destroy", "pp_driver_open", "pp_driver_close", "pp_driver_phase",
-           "pp_driver_prepare", "pp_driver_absorb", "pp_driver_tick"]
+           "pp_driver_prepare", "pp_driver_absorb", "pp_driver_tick", "pp_session_sampling",
+           "pp_sample"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -64,6 +65,18 @@ PP_FLAG_CUDA_CORE_GEMM = 0x1
 PP_FLAG_NO_PDL = 0x2
 PP_FLAG_TWO_GROUPS = 0x4
 PP_FLAG_SKIP_USER_STEPS = 0x8
+
+
+class pp_sampling(ctypes.Structure):
+    """Per-session sampling parameters (temperature <= 0 keeps a stream greedy)."""
+    _fields_ = [("text_temperature", ctypes.c_float), ("text_top_k", ctypes.c_int32),
+                ("text_top_p", ctypes.c_float), ("repetition_penalty", ctypes.c_float),
+                ("penalty_window", ctypes.c_int32), ("audio_temperature", ctypes.c_float),
+                ("audio_top_k", ctypes.c_int32), ("audio_top_p", ctypes.c_float),
+                ("seed", ctypes.c_uint64)]
+
+
+SAMPLE_HISTORY = 256   # the longest repetition-penalty window
 
 
 class pp_weights(ctypes.Structure):
@@ -133,6 +146,11 @@ def lib():
         L.pp_driver_absorb.argtypes = [P, P, P, P]
         L.pp_driver_absorb.restype = I
         L.pp_driver_tick.argtypes = [P, P, P, P, P, P]
+        L.pp_session_sampling.argtypes = [P, I, ctypes.POINTER(pp_sampling)]
+        L.pp_session_sampling.restype = I
+        F = ctypes.c_float
+        L.pp_sample.argtypes = [P, I64, I, I, F, I, F, F, P, I, P, P, P, P, P]
+        L.pp_sample.restype = I
         L.pp_driver_tick.restype = I
         _lib = L
     return _lib
@@ -347,6 +365,28 @@ def pp_rvq_dequantize(codes, code_stride, n_frames, n_books, codebooks, card, di
         codes, code_stride, n_frames, n_books, codebooks, card, dim, out, status, stream))
 
 
+def pp_session_sampling(h, slot, params=None):
+    """Sampling parameters of an open slot (a pp_sampling, or None for greedy)."""
+    return _check("pp_session_sampling", lib().pp_session_sampling(
+        h, slot, None if params is None else ctypes.byref(params)))
+
+
+def pp_sample(logits, ld, rows, n, temperature, top_k, top_p, penalty, hist, hist_ld, hist_n,
+              uniforms, tokens, status, stream):
+    """One token per row of device logits with the caller's uniforms (device pointers)."""
+    return _check("pp_sample", lib().pp_sample(logits, ld, rows, n, temperature, top_k, top_p,
+                                               penalty, hist, hist_ld, hist_n, uniforms, tokens,
+                                               status, stream))
+
+
+def sampling(text_temperature=0.0, text_top_k=0, text_top_p=1.0, repetition_penalty=1.0,
+             penalty_window=0, audio_temperature=0.0, audio_top_k=0, audio_top_p=1.0, seed=0):
+    """A pp_sampling with greedy defaults."""
+    return pp_sampling(text_temperature, text_top_k, text_top_p, repetition_penalty,
+                       penalty_window, audio_temperature, audio_top_k, audio_top_p,
+                       int(seed) & (2**64 - 1))
+
+
 # ---- convenience wrapper over torch device memory ---------------------------------------
 
 class Engine:
@@ -393,6 +433,13 @@ class Engine:
 
     def close(self, slot):
         pp_session_close(self.h, slot)
+
+    def set_sampling(self, slot, params=None, **kw):
+        """Sampling parameters of an open slot: a pp_sampling, keyword fields of one, or
+        nothing for greedy."""
+        if params is None and kw:
+            params = sampling(**kw)
+        pp_session_sampling(self.h, slot, params)
 
     def import_session(self, slot, pos):
         pp_session_import(self.h, slot, pos)

@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include "pp_internal.cuh"
+#include "pp_sample.cuh"
 
 namespace pp {
 
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b, const float* a
     if (c & 2) {             // (re)open: set the position once, then clear the request
       b.pos[s] = b.ctl_pos[s];
       b.ctl[s] = c & 1;
+      b.hist_len[s] = 0;     // a new session starts without text history
     }
     b.live[s] = c & 1;
     live_s = c & 1;
@@ -240,32 +242,50 @@ __device__ int block_argmax(const float* __restrict__ lg, int n, uint32_t* statu
 }
 
 __global__ void __launch_bounds__(1024) k_text_argmax(Dims D, Buffers b) {
+  extern __shared__ float s_row[];
   pdl_wait_and_trigger();
   const int s = blockIdx.x;
   if (!b.live[s]) {
     if (threadIdx.x == 0) { b.out_col[s * kRows] = -1; b.tok[s] = 0; }
     return;
   }
-  const int am = block_argmax(b.logits + (size_t)s * D.logits_ld, D.Vt, b.status);
+  const float* lg = b.logits + (size_t)s * D.logits_ld;
+  const SampleParams& sp = b.samp[s];
+  const bool forced = b.in_fmask[s * kRows] != 0;
+  const int pos = b.pos[s];
+  int am;
+  if (D.samp_text && sp.t_temp > 0.f && !forced) {
+    const uint64_t seed = ((uint64_t)sp.seed_hi << 32) | sp.seed_lo;
+    const int nh = sp.penalty != 1.f ? min(sp.window, b.hist_len[s]) : 0;
+    am = block_sample<1024>(lg, D.Vt, sp.t_temp, sp.t_top_k, sp.t_top_p, sp.penalty,
+                            b.hist + (size_t)s * kHist, nh, pos, samp::uniform(seed, pos, 0),
+                            b.status, s_row);
+  } else {
+    am = block_argmax(lg, D.Vt, b.status);
+  }
   if (threadIdx.x == 0) {
     int t = am;
-    if (b.in_fmask[s * kRows]) {
+    if (forced) {
       t = b.in_forced[s * kRows];
       if (t < 0 || t > D.Vt) { atomicOr(b.status, PP_S_INDEX); t = D.Vt; }
     }
     b.out_col[s * kRows] = t;
     b.tok[s] = t;
+    b.hist[(size_t)s * kHist + (pos & (kHist - 1))] = t;   // the repetition-penalty window
+    b.hist_len[s] = min(b.hist_len[s] + 1, kHist);
   }
 }
 
 cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s) {
-  { cudaError_t e_ = launch_k(k_text_argmax, dim3(D.B), dim3(1024), 0, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
+  const size_t smem = D.samp_text ? (size_t)D.Vt * sizeof(float) : 0;
+  { cudaError_t e_ = launch_k(k_text_argmax, dim3(D.B), dim3(1024), smem, s, 1, D, b); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
 }
 
 // Step k of the depformer decides row k+1: agent rows 1..8 are greedy unless forced,
 // user rows 9..16 take this frame's user codes.
 __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step) {
+  extern __shared__ float s_row[];
   pdl_wait_and_trigger();
   const int s = blockIdx.x, row = step + 1;
   if (!b.live[s]) {
@@ -273,9 +293,18 @@ __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step
     return;
   }
   int t = 0;
-  if (row <= PP_AGENT_ROWS && !b.in_fmask[s * kRows + row])
-    t = block_argmax(b.logits + (size_t)s * D.logits_ld + D.Vt + (size_t)step * D.Va, D.Va,
-                     b.status);
+  if (row <= PP_AGENT_ROWS && !b.in_fmask[s * kRows + row]) {
+    const float* lg = b.logits + (size_t)s * D.logits_ld + D.Vt + (size_t)step * D.Va;
+    const SampleParams& sp = b.samp[s];
+    if (D.samp_audio && sp.a_temp > 0.f) {
+      const uint64_t seed = ((uint64_t)sp.seed_hi << 32) | sp.seed_lo;
+      const int pos = b.pos[s];
+      t = block_sample<1024>(lg, D.Va, sp.a_temp, sp.a_top_k, sp.a_top_p, 1.f, nullptr, 0, -1,
+                             samp::uniform(seed, pos, row), b.status, s_row);
+    } else {
+      t = block_argmax(lg, D.Va, b.status);
+    }
+  }
   if (threadIdx.x == 0) {
     if (row <= PP_AGENT_ROWS) {
       if (b.in_fmask[s * kRows + row]) t = b.in_forced[s * kRows + row];
@@ -289,8 +318,51 @@ __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step
 }
 
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s) {
-  { cudaError_t e_ = launch_k(k_dep_argmax, dim3(D.B), dim3(1024), 0, s, 1, D, b, step); if (e_ != cudaSuccess) return e_; }
+  const size_t smem = D.samp_audio ? (size_t)D.Va * sizeof(float) : 0;
+  { cudaError_t e_ = launch_k(k_dep_argmax, dim3(D.B), dim3(1024), smem, s, 1, D, b, step); if (e_ != cudaSuccess) return e_; }
   return cudaGetLastError();
+}
+
+// Rows of logits sampled independently with the caller's uniforms (pp_sample).
+__global__ void __launch_bounds__(1024)
+    k_sample_rows(const float* __restrict__ logits, int64_t ld, int n, float temperature,
+                  int top_k, float top_p, float penalty, const int32_t* __restrict__ hist,
+                  int hist_ld, const int32_t* __restrict__ hist_n,
+                  const float* __restrict__ uniforms, int32_t* __restrict__ tokens,
+                  uint32_t* status) {
+  extern __shared__ float s_row[];
+  pdl_wait_and_trigger();
+  const int r = blockIdx.x;
+  const int nh = hist ? max(0, min(hist_n[r], hist_ld)) : 0;
+  const int t = block_sample<1024>(logits + (size_t)r * ld, n, temperature, top_k, top_p, penalty,
+                                   hist ? hist + (size_t)r * hist_ld : nullptr, nh, -1,
+                                   uniforms[r], status, s_row);
+  if (threadIdx.x == 0) tokens[r] = t;
+}
+
+cudaError_t launch_sample_rows(const float* logits, int64_t ld, int rows, int n, float temperature,
+                               int top_k, float top_p, float penalty, const int32_t* hist,
+                               int hist_ld, const int32_t* hist_n, const float* uniforms,
+                               int32_t* tokens, uint32_t* status, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_sample_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSampleSmemMax);
+  if (e != cudaSuccess) return e;
+  e = launch_k(k_sample_rows, dim3(rows), dim3(1024), (size_t)n * sizeof(float), s, 1, logits, ld,
+               n, temperature, top_k, top_p, penalty, hist, hist_ld, hist_n, uniforms, tokens,
+               status);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t sample_setup(const Dims& D) {
+  cudaError_t e = cudaSuccess;
+  if (D.samp_text)
+    e = cudaFuncSetAttribute(k_text_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             D.Vt * (int)sizeof(float));
+  if (e == cudaSuccess && D.samp_audio)
+    e = cudaFuncSetAttribute(k_dep_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             D.Va * (int)sizeof(float));
+  return e;
 }
 
 // ---- depformer step attention ------------------------------------------------------------

@@ -3,10 +3,13 @@
 #include <math.h>
 #include <string.h>
 
+#include <cmath>
+
 #include <new>
 #include <vector>
 
 #include "pp_internal.cuh"
+#include "pp_sample.cuh"
 
 using namespace pp;
 
@@ -81,6 +84,8 @@ struct pp_engine {
   Prof prof;
   std::vector<int32_t> ctl, ctl_pos;   // uploaded before the next tick when dirty
   bool ctl_dirty = false;
+  std::vector<SampleParams> samp;      // per-slot sampling parameters, uploaded when dirty
+  bool samp_dirty = false;
   std::vector<int64_t> pos;            // host mirror of each open slot's position
   std::vector<uint8_t> open;
 };
@@ -115,6 +120,8 @@ Dims make_dims(const pp_config* c) {
   D.nc_max = (c->window + kAttnChunk - 1) / kAttnChunk;
   D.logits_ld = c->text_vocab + c->n_q * c->audio_card;
   D.dep_steps = (c->flags & PP_FLAG_SKIP_USER_STEPS) ? c->n_q / 2 : c->n_q;
+  D.samp_text = (int64_t)c->text_vocab * 4 <= kSampleSmemMax;
+  D.samp_audio = (int64_t)c->audio_card * 4 <= kSampleSmemMax;
   return D;
 }
 
@@ -149,6 +156,9 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
   sh.ctl = cv.take<int32_t>(B);
   sh.ctl_pos = cv.take<int32_t>(B);
   sh.status = cv.take<uint32_t>(1);
+  sh.samp = cv.take<SampleParams>(B);
+  sh.hist_len = cv.take<int32_t>(B);
+  sh.hist = cv.take<int32_t>(B * kHist);
   sh.in_col = cv.take<int32_t>(B * kRows);
   sh.in_user = cv.take<int32_t>(B * PP_USER_ROWS);
   sh.in_fmask = cv.take<uint8_t>(B * kRows);
@@ -169,6 +179,9 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
       b.nvalid = sh.nvalid + slot0;
       b.ctl = sh.ctl + slot0;
       b.ctl_pos = sh.ctl_pos + slot0;
+      b.samp = sh.samp + slot0;
+      b.hist_len = sh.hist_len + slot0;
+      b.hist = sh.hist + (size_t)slot0 * kHist;
       b.in_col = sh.in_col + (size_t)slot0 * kRows;
       b.in_user = sh.in_user + (size_t)slot0 * PP_USER_ROWS;
       b.in_fmask = sh.in_fmask + (size_t)slot0 * kRows;
@@ -740,11 +753,12 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   e->ctl_pos.assign(e->B, 0);
   e->pos.assign(e->B, 0);
   e->open.assign(e->B, 0);
+  e->samp.assign(e->B, SampleParams{});
 
   e->tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
   g_use_pdl = !(c->flags & PP_FLAG_NO_PDL);   // read while this engine's graphs are captured
   cudaError_t err = cudaSuccess;
-  {  // zero the per-slot state (positions, liveness, control, status)
+  {  // zero the per-slot state (positions, liveness, control, status, sampling, history)
     const Buffers& sh = e->shared;
     err = cudaMemset(sh.pos, 0, (size_t)(reinterpret_cast<char*>(sh.in_col) -
                                           reinterpret_cast<char*>(sh.pos)));
@@ -769,6 +783,7 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
       if (!gr->has_amaps) err = cudaErrorInvalidValue;
     }
   }
+  for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) err = sample_setup(e->grp[g].D);
   if (err == cudaSuccess && e->tensor) {
     int dev = 0, nsm = 0;
     err = cudaGetDevice(&dev);
@@ -839,6 +854,8 @@ static int open_at(pp_engine* e, int slot, int64_t pos) {
   e->ctl_pos[slot] = (int32_t)pos;
   e->ctl_dirty = true;
   e->pos[slot] = pos;
+  e->samp[slot] = SampleParams{};   // a new session starts greedy
+  e->samp_dirty = true;
   return PP_OK;
 }
 
@@ -853,6 +870,41 @@ int pp_session_close(pp_engine* e, int slot) {
   e->open[slot] = 0;
   e->ctl[slot] = 0;
   e->ctl_dirty = true;
+  e->samp[slot] = SampleParams{};
+  e->samp_dirty = true;
+  return PP_OK;
+}
+
+int pp_session_sampling(pp_engine* e, int slot, const pp_sampling* p) {
+  if (!e) return PP_EINVAL;
+  if (slot < 0 || slot >= e->B) return PP_E_RANGE;
+  if (!e->open[slot]) return PP_E_NOTLIVE;
+  SampleParams sp{};
+  if (p) {
+    const float fs[] = {p->text_temperature, p->text_top_p, p->repetition_penalty,
+                        p->audio_temperature, p->audio_top_p};
+    for (float f : fs)
+      if (!std::isfinite(f)) return PP_EINVAL;
+    if (!(p->text_top_p > 0.f && p->text_top_p <= 1.f)) return PP_EINVAL;
+    if (!(p->audio_top_p > 0.f && p->audio_top_p <= 1.f)) return PP_EINVAL;
+    if (!(p->repetition_penalty > 0.f)) return PP_EINVAL;
+    if (p->penalty_window < 0 || p->penalty_window > kHist) return PP_EINVAL;
+    const Dims& D = e->grp[0].D;
+    if (p->text_temperature > 0.f && !D.samp_text) return PP_EINVAL;
+    if (p->audio_temperature > 0.f && !D.samp_audio) return PP_EINVAL;
+    sp.t_temp = p->text_temperature;
+    sp.t_top_k = p->text_top_k;
+    sp.t_top_p = p->text_top_p;
+    sp.penalty = p->repetition_penalty;
+    sp.window = p->penalty_window;
+    sp.a_temp = p->audio_temperature;
+    sp.a_top_k = p->audio_top_k;
+    sp.a_top_p = p->audio_top_p;
+    sp.seed_lo = (uint32_t)p->seed;
+    sp.seed_hi = (uint32_t)(p->seed >> 32);
+  }
+  e->samp[slot] = sp;
+  e->samp_dirty = true;
   return PP_OK;
 }
 
@@ -901,6 +953,10 @@ static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* us
     err = cudaMemcpyAsync(b.ctl, e->ctl.data(), B * 4, cudaMemcpyHostToDevice, s);
   if (err == cudaSuccess && upload)
     err = cudaMemcpyAsync(b.ctl_pos, e->ctl_pos.data(), B * 4, cudaMemcpyHostToDevice, s);
+  const bool upload_samp = e->samp_dirty;
+  if (err == cudaSuccess && upload_samp)
+    err = cudaMemcpyAsync(b.samp, e->samp.data(), B * sizeof(SampleParams), cudaMemcpyHostToDevice,
+                          s);
   if (err == cudaSuccess) err = cudaGraphLaunch(exec, s);
   if (err == cudaSuccess)
     err = cudaMemcpyAsync(column, b.out_col, B * kRows * 4, cudaMemcpyDefault, s);
@@ -912,6 +968,7 @@ static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* us
     for (size_t i = 0; i < B; ++i) e->ctl[i] &= 1;   // the device applies a reset once
     e->ctl_dirty = false;
   }
+  if (upload_samp) e->samp_dirty = false;
   for (size_t i = 0; i < B; ++i)
     if (e->open[i]) e->pos[i] += 1;
   return PP_OK;
@@ -984,6 +1041,26 @@ int pp_status(pp_engine* e, void* stream, uint32_t* bits) {
 }
 
 int pp_step_kernel_count(pp_engine* e) { return e ? e->n_kernels : PP_EINVAL; }
+
+int pp_sample(const float* logits, int64_t ld, int rows, int n, float temperature, int top_k,
+              float top_p, float penalty, const int32_t* hist, int hist_ld,
+              const int32_t* hist_n, const float* uniforms, int32_t* tokens, uint32_t* status,
+              void* stream) {
+  if (rows < 0 || n < 1 || ld < n || (int64_t)n * 4 > kSampleSmemMax) return PP_EINVAL;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return PP_EINVAL;
+  if (!(top_p > 0.f && top_p <= 1.f) || !(penalty > 0.f) || !std::isfinite(penalty))
+    return PP_EINVAL;
+  if (hist && (!hist_n || hist_ld < 1 || hist_ld > kHist)) return PP_EINVAL;
+  if (rows == 0) return PP_OK;
+  if (!logits || !uniforms || !tokens) return PP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(uniforms) |
+       reinterpret_cast<uintptr_t>(tokens)) & 3)
+    return PP_EINVAL;
+  const cudaError_t err =
+      launch_sample_rows(logits, ld, rows, n, temperature, top_k, top_p, penalty, hist, hist_ld,
+                         hist_n, uniforms, tokens, status, (cudaStream_t)stream);
+  return err == cudaSuccess ? PP_OK : PP_E_CUDA;
+}
 
 static bool ring_attention_args_ok(int B, int H, int head_dim, int window) {
   return B >= 1 && H >= 1 && window >= 1 && head_dim_ok(head_dim) &&

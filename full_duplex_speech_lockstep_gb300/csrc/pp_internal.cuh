@@ -28,6 +28,8 @@ struct Dims {
   int logits_ld;         // Vt + nq * Va
   int Bp;                // slots padded to a multiple of 8: operand rows are [hi: Bp][lo: Bp]
   int dep_steps;         // depformer steps run (n_q, or n_q / 2 when the user rows are elided)
+  int samp_text;         // 1: the text decision kernel holds a logit row in shared memory
+  int samp_audio;        // 1: the same for the agent audio rows
 };
 
 struct Buffers {
@@ -61,6 +63,9 @@ struct Buffers {
   int32_t* ctl;            // [B] host-uploaded control: bit0 live, bit1 reset position
   int32_t* ctl_pos;        // [B] position applied when bit1 is set
   uint32_t* status;        // [1]
+  struct SampleParams* samp;   // [B] sampling parameters (greedy when temperature <= 0)
+  int32_t* hist_len;       // [B] text tokens recorded since open (capped at kHist)
+  int32_t* hist;           // [B][kHist] text token of position p at p mod kHist
   // per-tick inputs / outputs (staged)
   int32_t* in_col;         // [B][17]
   int32_t* in_user;        // [B][8]
@@ -278,6 +283,11 @@ cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
                             cudaStream_t s);
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s);
+cudaError_t sample_setup(const Dims& D);   // shared-memory opt-in of the decision kernels
+cudaError_t launch_sample_rows(const float* logits, int64_t ld, int rows, int n, float temperature,
+                               int top_k, float top_p, float penalty, const int32_t* hist,
+                               int hist_ld, const int32_t* hist_n, const float* uniforms,
+                               int32_t* tokens, uint32_t* status, cudaStream_t s);
 cudaError_t launch_finish(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_user_rows(const Dims& D, const Buffers& b, cudaStream_t s);
 

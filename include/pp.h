@@ -164,6 +164,62 @@ int pp_session_import(pp_engine* e, int slot, int64_t pos);
  * mirror.  Errors: PP_E_RANGE, PP_E_NOTLIVE. */
 int pp_session_pos(pp_engine* e, int slot, int64_t* pos);
 
+/* ---- sampling variants -------------------------------------------------------------
+ * The pages decode greedily ("PersonaPlex ... vLLM-Omni", greedy decoding and parity:
+ * the parity gates pin greedy output) and list the knobs a deployment may turn instead:
+ * temperature, nucleus top-p and a repetition penalty for the text stream, a separate
+ * audio temperature (deployment config; the persona-tuning article's generation
+ * parameters).  A row that is sampled takes these steps in order:
+ *   1. repetition penalty (text only): each distinct token among the session's last
+ *      penalty_window text tokens has its logit divided by R when positive and
+ *      multiplied by R otherwise (Keskar et al., CTRL, 2019);
+ *   2. division by the temperature;
+ *   3. top-k: keep the values at or above the k-th largest (ties kept);
+ *   4. e_i = exp(v_i - max v) over the kept values;
+ *   5. nucleus: keep e at or above the largest e value whose own mass plus the mass of
+ *      every larger e reaches top_p * sum(e) (ties kept);
+ *   6. inverse CDF in index order: the first kept token whose running mass exceeds
+ *      u * (kept mass).
+ * u is drawn from Philox4x64-10 (Salmon et al., SC 2011) under the key (seed, 0) at the
+ * counter (position, row / 4, 0, 0): the top 24 bits of word row % 4, times 2^-24,
+ * where row is 0 for text and 1..8 for the agent audio codebooks and position is the
+ * session's position of the tick.  A session's draws thus depend on its seed and
+ * position only, never on its slot.  Forced rows draw nothing.  Logits that are not
+ * finite are never chosen.  Every decision is deterministic (fixed reduction orders). */
+typedef struct {
+  float text_temperature;    /* <= 0: the text row stays greedy (the default) */
+  int32_t text_top_k;        /* <= 0: no top-k filter */
+  float text_top_p;          /* in (0, 1]; 1: no nucleus filter */
+  float repetition_penalty;  /* > 0; 1: off */
+  int32_t penalty_window;    /* last N text tokens of the session, 0..256 */
+  float audio_temperature;   /* <= 0: the agent audio rows stay greedy (the default) */
+  int32_t audio_top_k;       /* <= 0: no top-k filter */
+  float audio_top_p;         /* in (0, 1]; 1: no nucleus filter */
+  uint64_t seed;             /* the session's random stream */
+} pp_sampling;
+
+/* Set the sampling parameters of open slot `slot` from its next tick on (NULL: greedy,
+ * which is also the state after pp_session_open).  The text history behind the
+ * penalty counts every text token of the session since open, forced ones included.
+ * Errors: PP_E_RANGE, PP_E_NOTLIVE, PP_EINVAL (a NaN or out-of-range field, or text
+ * sampling on a vocabulary above 51200 / audio sampling on a codebook above 51200). */
+int pp_session_sampling(pp_engine* e, int slot, const pp_sampling* p);
+
+/* Sample one token per row of device logits with caller-given uniforms, by the steps
+ * above (the kernel the tick runs for a sampled row), asynchronous on `stream`:
+ *   logits    f32 [rows, ld], row r's n logits at r*ld (n <= ld, n <= 51200)
+ *   hist      int32 [rows, hist_ld] history tokens (order irrelevant) or NULL;
+ *             hist_n int32 [rows] how many of row r's entries count (<= hist_ld <= 256)
+ *   uniforms  f32 [rows] in [0, 1)
+ *   tokens    int32 [rows] out
+ *   status    optional device word; PP_S_NAN is OR-ed in when a row held NaN
+ * temperature > 0, top_p in (0, 1], penalty > 0.  rows == 0 does nothing.
+ * Errors: PP_EINVAL, PP_E_CUDA. */
+int pp_sample(const float* logits, int64_t ld, int rows, int n, float temperature, int top_k,
+              float top_p, float penalty, const int32_t* hist, int hist_ld,
+              const int32_t* hist_n, const float* uniforms, int32_t* tokens, uint32_t* status,
+              void* stream);
+
 /* Device address of one ring block: layer `layer`, slot `slot`, kv = 0 (K, stored
  * after RoPE) or 1 (V); the block is bf16 [n_heads, window, head_dim], contiguous.
  * Errors: PP_E_RANGE, PP_EINVAL. */

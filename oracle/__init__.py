@@ -76,7 +76,7 @@ def lib():
         L.ora_sample_uniform.restype = ctypes.c_float
         L.ora_sample.argtypes = [P, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float,
                                  ctypes.c_float, P, ctypes.c_int, ctypes.c_float,
-                                 ctypes.c_double, P, P]
+                                 ctypes.c_double, P, P, P]
         L.ora_sample.restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -262,22 +262,29 @@ def sample_uniform(seed, pos, row):
     return float(lib().ora_sample_uniform(int(seed) & (2**64 - 1), int(pos), int(row)))
 
 
-# relative distance to a decision boundary below which fp32 masses and expf on the GPU
-# may take either side (the masses carry well under 1e-5 relative rounding error)
-SAMPLE_TOL = 1e-4
+# Relative distance to a decision boundary within which an fp32 evaluation may decide
+# either way.  The GPU sums a row of <= 51200 non-negative terms as sequential chunks of
+# <= 50 per thread, a 5-level warp scan or butterfly, an ordered sum of 32 warp totals
+# and two more additions: relative error below (49 + 5 + 31 + 2) * 2^-24 = 5.2e-6; its
+# expf and the oracle's differ by at most 3 ulp (3.6e-7 relative) per term.
+SAMPLE_TOL = 6e-6
 
 
 def sample(logits, u, temperature=1.0, top_k=0, top_p=1.0, penalty=1.0, history=(),
            tol=SAMPLE_TOL):
-    """One sampled token from fp32 logits -> (token, ambiguous, n_kept)."""
+    """One sampled token from fp32 logits -> (token, alternatives, n_kept): the
+    alternatives are every token the steps give with the target moved by tol or the
+    nucleus cut moved by one run where that close (the token itself included)."""
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     h = np.ascontiguousarray(np.asarray(history, dtype=np.int32).reshape(-1))
-    amb = ctypes.c_int(0)
     kept = ctypes.c_int(0)
+    alts = np.zeros(9, np.int32)
+    na = ctypes.c_int(0)
     t = lib().ora_sample(lg.ctypes.data, lg.size, float(temperature), int(top_k), float(top_p),
                          float(penalty), h.ctypes.data if h.size else None, int(h.size),
-                         float(u), float(tol), ctypes.byref(amb), ctypes.byref(kept))
-    return int(t), bool(amb.value), int(kept.value)
+                         float(u), float(tol), ctypes.byref(kept), alts.ctypes.data,
+                         ctypes.byref(na))
+    return int(t), set(int(x) for x in alts[:na.value]), int(kept.value)
 
 
 def initial_column(shape):

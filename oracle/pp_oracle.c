@@ -394,13 +394,40 @@ static int cmp_f32_desc(const void* a, const void* b) {
   return (x < y) - (x > y);
 }
 
+/* Step 6 for one threshold: the first index e >= tp (e > 0) whose running mass
+ * exceeds (u + shift) * (kept mass), else the last such index (-1: none). */
+static int32_t inverse_cdf(const float* e, int n, float tp, double u, double shift) {
+  double ZK = 0.0;
+  int last = -1;
+  for (int i = 0; i < n; ++i)
+    if (e[i] > 0.f && e[i] >= tp) {
+      ZK += (double)e[i];
+      last = i;
+    }
+  const double target = (u + shift) * ZK;
+  double run = 0.0;
+  for (int i = 0; i < n; ++i) {
+    if (!(e[i] > 0.f && e[i] >= tp)) continue;
+    run += (double)e[i];
+    if (run > target) return i;
+  }
+  return last;
+}
+
+static void add_alt(int32_t tok, int32_t* alts, int* n_alts) {
+  for (int i = 0; i < *n_alts; ++i)
+    if (alts[i] == tok) return;
+  if (*n_alts < ORA_SAMPLE_MAX_ALTS) alts[(*n_alts)++] = tok;
+}
+
 int32_t ora_sample(const float* logits, int n, float temperature, int top_k, float top_p,
                    float penalty, const int32_t* hist, int n_hist, float u, double tol,
-                   int* ambiguous, int* n_kept) {
+                   int* n_kept, int32_t* alts, int* n_alts) {
   float* v = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
   float* e = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
   float* srt = (float*)malloc(sizeof(float) * (n > 0 ? n : 1));
-  int amb = 0;
+  int na = 0;
+  int32_t alt_buf[ORA_SAMPLE_MAX_ALTS];
   for (int i = 0; i < n; ++i) v[i] = logits[i];
   /* 1. repetition penalty, once per distinct history token */
   for (int j = 0; j < n_hist; ++j) {
@@ -423,8 +450,9 @@ int32_t ora_sample(const float* logits, int n, float temperature, int top_k, flo
   }
   if (n_fin == 0) {
     free(v); free(e); free(srt);
-    if (ambiguous) *ambiguous = 0;
     if (n_kept) *n_kept = 0;
+    if (n_alts) *n_alts = 1;
+    if (alts) alts[0] = 0;
     return 0;
   }
   /* 3. top-k threshold: the k-th largest finite value */
@@ -440,8 +468,10 @@ int32_t ora_sample(const float* logits, int n, float temperature, int top_k, flo
     Z += (double)e[i];
   }
   /* 5. nucleus threshold: walk the e values from the largest down, a run of equal
-   * values at a time, until the mass reaches p * Z */
-  float tp = 0.f;
+   * values at a time, until the mass reaches p * Z.  Near the cut the GPU's fp32
+   * masses (relative error below tol) or its expf (a few ulp, below 1e-6 relative)
+   * may cut one run earlier or later: those thresholds are kept as alternatives. */
+  float tp = 0.f, tp_alt[2] = {-1.f, -1.f};
   if (top_p < 1.f) {
     int ne = 0;
     for (int i = 0; i < n; ++i)
@@ -457,38 +487,28 @@ int32_t ora_sample(const float* logits, int n, float temperature, int top_k, flo
       while (j < ne && srt[j] == val) mass += (double)srt[j++];
       if (mass >= P) {
         tp = val;
-        /* near the cut the GPU's fp32 masses and expf may land on either side */
-        if (mass - P < tol * Z || P - before < tol * Z) amb = 1;
-        if (j < ne && (double)srt[j] >= (double)val * (1.0 - tol)) amb = 1;
-        if (start > 0 && (double)srt[start - 1] <= (double)val * (1.0 + tol)) amb = 1;
+        if (j < ne && (mass - P < tol * Z || (double)srt[j] >= (double)val * (1.0 - 1e-6)))
+          tp_alt[0] = srt[j];                          /* one run later */
+        if (start > 0 && (P - before < tol * Z || (double)srt[start - 1] <= (double)val * (1.0 + 1e-6)))
+          tp_alt[1] = srt[start - 1];                  /* one run earlier */
         break;
       }
     }
   }
   /* 6. inverse CDF in index order over the kept set */
-  double ZK = 0.0;
-  int last = -1, kept = 0;
-  for (int i = 0; i < n; ++i)
-    if (e[i] > 0.f && e[i] >= tp) {
-      ZK += (double)e[i];
-      last = i;
-      ++kept;
-    }
-  const double target = (double)u * ZK;
-  double run = 0.0;
-  int tok = last;
-  for (int i = 0; i < n; ++i) {
-    if (!(e[i] > 0.f && e[i] >= tp)) continue;
-    const double before = run;
-    run += (double)e[i];
-    if (run > target) {
-      tok = i;
-      if (run - target < tol * ZK || target - before < tol * ZK) amb = 1;
-      break;
-    }
-  }
+  const int32_t tok = inverse_cdf(e, n, tp, (double)u, 0.0);
+  add_alt(tok, alt_buf, &na);
+  add_alt(inverse_cdf(e, n, tp, (double)u, -tol), alt_buf, &na);
+  add_alt(inverse_cdf(e, n, tp, (double)u, tol), alt_buf, &na);
+  for (int a = 0; a < 2; ++a)
+    if (tp_alt[a] >= 0.f)
+      for (int d = -1; d <= 1; ++d) add_alt(inverse_cdf(e, n, tp_alt[a], (double)u, d * tol), alt_buf, &na);
+  int kept = 0;
+  for (int i = 0; i < n; ++i) kept += (e[i] > 0.f && e[i] >= tp);
   free(v); free(e); free(srt);
-  if (ambiguous) *ambiguous = amb;
   if (n_kept) *n_kept = kept;
+  if (alts)
+    for (int i = 0; i < na; ++i) alts[i] = alt_buf[i] < 0 ? 0 : alt_buf[i];
+  if (n_alts) *n_alts = na;
   return tok < 0 ? 0 : tok;
 }

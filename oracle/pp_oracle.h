@@ -118,14 +118,17 @@ void ora_rvq_dequantize(const int32_t* codes, int code_stride, int n_frames, int
                         const float* codebooks, int card, int dim, double* out, int* bad);
 
 /* Sampling variants (the reading is stated at the definitions in pp_oracle.c).
- * ora_sample returns the token; *ambiguous is set when the decision lies within tol
- * (relative) of a boundary that fp32 masses or expf could move, *n_kept counts the
- * tokens left after the filters. */
+ * ora_sample returns the token and, in alts[0 .. *n_alts), every token that the same
+ * steps give when the draw's target moves by tol (relative to the kept mass) or the
+ * nucleus cut moves by one run where its mass or value lies that close to the cut:
+ * the decisions an fp32 evaluation of the steps may reach.  *n_kept counts the tokens
+ * left after the filters. */
+#define ORA_SAMPLE_MAX_ALTS 9
 void ora_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
 float ora_sample_uniform(uint64_t seed, int64_t pos, int row);
 int32_t ora_sample(const float* logits, int n, float temperature, int top_k, float top_p,
                    float penalty, const int32_t* hist, int n_hist, float u, double tol,
-                   int* ambiguous, int* n_kept);
+                   int* n_kept, int32_t* alts, int* n_alts);
 
 void ora_step(const ora_shape* s, const ora_weights* w, ora_session* sess,
               const int32_t* prev_column, const int32_t* user_codes,

@@ -76,3 +76,28 @@ def test_create_rejects_bad_arguments_without_touching_the_gpu():
     assert lib.pp_create(ctypes.byref(cfg), ctypes.byref(w), None, 0, ctypes.byref(h)) == pp.PP_EINVAL
     assert lib.pp_session_open(None, 0) == pp.PP_EINVAL
     assert lib.pp_step(None, None, None, None, None, None, None, None) == pp.PP_EINVAL
+
+
+def test_sampling_rejects_bad_arguments_without_touching_the_gpu():
+    lib = pp.lib()
+    S = pp.sampling(text_temperature=0.7, text_top_p=0.9, seed=3)
+    assert lib.pp_session_sampling(None, 0, ctypes.byref(S)) == pp.PP_EINVAL
+    # rows == 0 is a no-op; every malformed argument is refused before any CUDA call
+    ok = dict(ld=64, rows=0, n=64, T=0.7, k=0, p=0.9, R=1.0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.pp_sample(None, a["ld"], a["rows"], a["n"], a["T"], a["k"], a["p"], a["R"],
+                             None, 0, None, None, None, None, None)
+    assert call() == pp.PP_OK
+    assert call(rows=1) == pp.PP_EINVAL                 # null logits / uniforms / tokens
+    assert call(n=0) == pp.PP_EINVAL
+    assert call(ld=32) == pp.PP_EINVAL                  # n > ld
+    assert call(n=60000, ld=60000) == pp.PP_EINVAL      # a row larger than shared memory
+    assert call(T=0.0) == pp.PP_EINVAL
+    assert call(T=float("nan")) == pp.PP_EINVAL
+    assert call(p=0.0) == pp.PP_EINVAL
+    assert call(p=1.5) == pp.PP_EINVAL
+    assert call(R=0.0) == pp.PP_EINVAL
+    assert lib.pp_sample(None, 64, 0, 64, 0.7, 0, 0.9, 1.0, ctypes.c_void_p(16), 300, None,
+                         None, None, None, None) == pp.PP_EINVAL   # history without counts

@@ -1,0 +1,262 @@
+"""Sampling variants on the GPU against the oracle's sampler (GPU).
+
+Standalone (pp_sample): rows of seeded logits shaped like the text head (32000 wide)
+and the audio heads (2048 wide), plus a ragged tiny width, tie-heavy rows and rows with
+NaN / infinite entries, sampled with seeded uniforms on both sides from the SAME fp32
+logits.  The steps up to the temperature are single IEEE operations on both sides, so
+the filters see identical values; only expf and the fp32 mass sums differ.  The oracle
+returns its token and every token reachable with the target or the nucleus cut moved
+within SAMPLE_TOL (the bound on the GPU's fp32 rounding): the GPU's token must equal the
+oracle's where that set is one token, and lie in the set elsewhere.
+
+In the tick: sessions with their own parameters and seeds run beside a greedy one.
+Every tick the GPU's logits are checked against the oracle's step with the GPU's column
+forced (so both sides condition on the same tokens), and every sampled row's token is
+checked against the oracle's sampler on the GPU's own logits with the uniform the
+oracle draws for (seed, position, row).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from harness import LOGIT_TOL, device_weights, initial_column
+
+pytestmark = pytest.mark.gpu
+
+
+def _uniforms(n, seed, stream):
+    return synth.uniform_i32(n, seed, stream, 0, 1 << 24).astype(np.float64) / float(1 << 24)
+
+
+def _logit_rows(rows, n, seed, kind):
+    x = synth.normal_f32(rows * n, seed, 40, 1.3).reshape(rows, n)
+    if kind == "ties":
+        x = np.round(x * 2.0) / 2.0                # many exact ties at every cut
+    elif kind == "nonfinite":
+        idx = synth.uniform_i32(rows * 8, seed, 41, 0, n).reshape(rows, 8)
+        for r in range(rows):
+            x[r, idx[r, :3]] = np.nan
+            x[r, idx[r, 3:6]] = -np.inf
+    elif kind == "flat":
+        x[:] = 0.25
+    return np.ascontiguousarray(x, np.float32)
+
+
+def _run_gpu(lg, u, temperature, top_k, top_p, penalty, hist=None):
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    rows, n = lg.shape
+    d_lg = torch.from_numpy(lg).cuda()
+    d_u = torch.from_numpy(u.astype(np.float32)).cuda()
+    d_t = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hp = hn = None
+    hld = 0
+    if hist is not None:
+        hld = max(1, max(len(h) for h in hist))
+        ha = np.full((rows, hld), -1, np.int32)
+        for r, h in enumerate(hist):
+            ha[r, :len(h)] = h
+        hp = torch.from_numpy(ha).cuda()
+        hn = torch.tensor([len(h) for h in hist], dtype=torch.int32, device="cuda")
+    pp.pp_sample(d_lg.data_ptr(), n, rows, n, temperature, top_k, top_p, penalty,
+                 None if hp is None else hp.data_ptr(), hld,
+                 None if hn is None else hn.data_ptr(), d_u.data_ptr(), d_t.data_ptr(),
+                 st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return d_t.cpu().numpy(), int(st.item())
+
+
+CASES = [
+    # (n, kind, temperature, top_k, top_p, penalty)
+    (32000, "normal", 0.7, 0, 0.9, 1.0),
+    (32000, "normal", 1.0, 0, 1.0, 1.2),
+    (32000, "normal", 0.3, 250, 1.0, 1.0),
+    (32000, "ties", 0.8, 25, 0.95, 1.1),
+    (2048, "normal", 0.3, 0, 1.0, 1.0),
+    (2048, "normal", 0.8, 250, 0.8, 1.0),
+    (2048, "ties", 1.0, 0, 0.5, 1.0),
+    (2048, "nonfinite", 0.9, 100, 0.9, 1.0),
+    (37, "normal", 1.5, 5, 0.7, 1.3),
+    (37, "flat", 1.0, 0, 1.0, 1.0),
+    (1, "normal", 0.5, 0, 0.9, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "%d-%s-T%g-k%d-p%g-R%g" % c)
+def test_sample_rows_match_oracle(case):
+    n, kind, T, k, p, R = case
+    rows = 64
+    lg = _logit_rows(rows, n, 100 + n + int(T * 10), kind)
+    u = _uniforms(rows, 7, n)
+    hist = None
+    if R != 1.0:
+        hist = [list(synth.uniform_i32(1 + (r * 7) % 60, 9, 300 + r, 0, n)) for r in range(rows)]
+    got, st = _run_gpu(lg, u, T, k, p, R, hist)
+    amb_rows = 0
+    for r in range(rows):
+        want, alts, kept = oracle.sample(lg[r], np.float32(u[r]), T, k, p, R,
+                                         hist[r] if hist else ())
+        if len(alts) > 1:                    # within rounding of a boundary: any of these
+            amb_rows += 1
+            assert got[r] in alts, (r, got[r], alts)
+        else:
+            assert got[r] == want, (r, got[r], want, kept)
+    assert amb_rows <= (2 * rows) // 3       # most rows are compared exactly
+    assert bool(st & 1) == (kind == "nonfinite")   # PP_S_NAN only where NaN was present
+
+
+def test_sample_rows_limits_and_degenerate_rows():
+    n, rows = 2048, 16
+    lg = _logit_rows(rows, n, 5, "normal")
+    u = _uniforms(rows, 8, 1)
+    am = lg.argmax(axis=1)
+    assert np.array_equal(_run_gpu(lg, u, 1.0, 1, 1.0, 1.0)[0], am)        # top-k = 1
+    assert np.array_equal(_run_gpu(lg, u, 1.0, 0, 1e-6, 1.0)[0], am)       # tiny nucleus
+    assert np.array_equal(_run_gpu(lg, u, 1e-4, 0, 1.0, 1.0)[0], am)       # cold
+    bad = np.full((2, 64), np.nan, np.float32)
+    bad[1] = -np.inf
+    toks, st = _run_gpu(bad, u[:2], 1.0, 0, 0.9, 1.0)
+    assert list(toks) == [0, 0] and (st & 1)
+    # top_k beyond the row keeps everything: the same tokens as no top-k at all
+    assert np.array_equal(_run_gpu(lg, u, 0.9, 5000, 1.0, 1.0)[0], _run_gpu(lg, u, 0.9, 0, 1.0, 1.0)[0])
+
+
+def test_sample_rows_are_deterministic_and_row_independent():
+    n = 32000
+    lg = _logit_rows(8, n, 77, "normal")
+    u = _uniforms(8, 78, 1)
+    a, _ = _run_gpu(lg, u, 0.8, 0, 0.9, 1.0)
+    b, _ = _run_gpu(lg, u, 0.8, 0, 0.9, 1.0)
+    c, _ = _run_gpu(lg[3:4].copy(), u[3:4].copy(), 0.8, 0, 0.9, 1.0)
+    assert np.array_equal(a, b) and c[0] == a[3]
+
+
+# ---- in the tick ------------------------------------------------------------------------
+
+PARAMS = {
+    0: dict(text_temperature=0.8, text_top_p=0.9, repetition_penalty=1.3, penalty_window=6,
+            audio_temperature=0.5, audio_top_k=50, seed=11),
+    1: None,                                        # greedy neighbour
+    2: dict(text_temperature=1.2, text_top_k=20, audio_temperature=0.9, audio_top_p=0.8,
+            seed=2**63 + 5),
+}
+
+
+def _check_logits(got, want):
+    tol = LOGIT_TOL * float(np.std(want.astype(np.float64)))
+    assert float(np.max(np.abs(got.astype(np.float64) - want))) <= tol
+
+
+def test_tick_sampling_matches_oracle_decisions():
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    shape = synth.TINY
+    B, T = 3, 14
+    w_host = synth.make_weights_host(shape, 3)
+    eng = pp.Engine(shape, B, device_weights(w_host))
+    orc = oracle.Oracle(shape, w_host)
+    sess = {}
+    for s in range(B):
+        eng.open(s)
+        if PARAMS[s]:
+            eng.set_sampling(s, **PARAMS[s])
+        sess[s] = orc.new_session()
+    prev = np.stack([initial_column(shape)] * B)
+    hist = {s: [] for s in range(B)}
+    ld = eng.logits_ld
+    lg_d = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+    checked = differs = 0
+    for t in range(T):
+        user = synth.uniform_i32(B * 8, 50, 400 + t, 0, shape.audio_card).reshape(B, 8)
+        fmask = np.zeros((B, 17), np.uint8)
+        forced = np.zeros((B, 17), np.int32)
+        if 2 <= t <= 4:                             # slot 0: forced text (persona-like)
+            fmask[0, 0], forced[0, 0] = 1, 100 + t
+        col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda(),
+                       torch.from_numpy(fmask).cuda(), torch.from_numpy(forced).cuda(),
+                       logits=lg_d).cpu().numpy()
+        lg = lg_d.cpu().numpy()
+        for s in range(B):
+            g = col[s]
+            lt, la = lg[s, :shape.text_vocab], lg[s, shape.text_vocab:].reshape(16, -1)
+            all9 = np.zeros(17, np.uint8)
+            all9[:9] = 1
+            co, olt, ola = orc.step(sess[s], prev[s], user[s], all9, g.astype(np.int32))
+            assert np.array_equal(co, g)
+            _check_logits(lt, olt)
+            _check_logits(la, ola)
+            P = PARAMS[s]
+            decisions = []   # (row, logits, temperature, top_k, top_p, penalty, history)
+            if P is None:
+                assert g[0] == oracle.argmax_f32(lt) and all(
+                    g[r] == oracle.argmax_f32(la[r - 1]) for r in range(1, 9))
+            else:
+                if not fmask[s, 0]:
+                    decisions.append((0, lt, P.get("text_temperature"), P.get("text_top_k", 0),
+                                      P.get("text_top_p", 1.0), P.get("repetition_penalty", 1.0),
+                                      hist[s][-P.get("penalty_window", 0):] if P.get("penalty_window") else []))
+                else:
+                    assert g[0] == forced[s, 0]
+                for r in range(1, 9):
+                    decisions.append((r, la[r - 1], P["audio_temperature"], P.get("audio_top_k", 0),
+                                      P.get("audio_top_p", 1.0), 1.0, []))
+            for r, row_lg, Ts, k, p, R, h in decisions:
+                u = oracle.sample_uniform(P["seed"], t, r)
+                want, alts, _ = oracle.sample(row_lg, u, Ts, k, p, R, h)
+                assert g[r] in alts, (t, s, r, g[r], alts)
+                if len(alts) == 1:
+                    checked += 1
+                differs += int(g[r] != oracle.argmax_f32(row_lg))
+            assert np.array_equal(g[9:], user[s])
+            hist[s].append(int(g[0]))
+        prev = col.astype(np.int32)
+    assert checked >= 0.9 * T * 2 * 9 - 6
+    assert differs > 20                             # the sampled rows really left greedy
+
+
+def test_tick_sampling_is_slot_independent_and_reset_on_open():
+    """A session's columns depend on its seed, parameters and inputs only: the same
+    session in slot 2 of one engine (alone) and slot 0 of another (beside a sampled
+    neighbour in slot 1) is bit-identical; reopening a slot restores greedy decoding."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    shape = synth.TINY
+    w_host = synth.make_weights_host(shape, 4)
+    w_dev = device_weights(w_host)
+    P = dict(text_temperature=0.9, text_top_p=0.85, repetition_penalty=1.2, penalty_window=4,
+             audio_temperature=0.6, audio_top_k=100, seed=4242)
+    T = 10
+
+    def run(B, slot, neighbour):
+        eng = pp.Engine(shape, B, w_dev)
+        eng.open(slot)
+        eng.set_sampling(slot, **P)
+        if neighbour is not None:
+            eng.open(neighbour)
+            eng.set_sampling(neighbour, **dict(P, seed=1))
+        prev = np.stack([initial_column(shape)] * B)
+        cols = []
+        for t in range(T):
+            user = np.tile(synth.uniform_i32(8, 60, 500 + t, 0, shape.audio_card), (B, 1))
+            col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda()).cpu().numpy()
+            cols.append(col[slot].copy())
+            prev = col.astype(np.int32)
+            prev[prev < 0] = initial_column(shape)[np.where(prev < 0)[1]]
+        return np.stack(cols), eng
+
+    a, _ = run(4, 2, None)
+    b, eng = run(4, 0, 1)
+    assert np.array_equal(a, b)
+    # reopen slot 0: greedy again, like a fresh engine's slot
+    eng.close(0)
+    eng.open(0)
+    prev = np.stack([initial_column(shape)] * 4)
+    user = np.tile(synth.uniform_i32(8, 60, 500, 0, shape.audio_card), (4, 1))
+    lg = torch.empty((4, eng.logits_ld), dtype=torch.float32, device="cuda")
+    col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda(), logits=lg).cpu().numpy()
+    l0 = lg[0].cpu().numpy()
+    assert col[0, 0] == oracle.argmax_f32(l0[:shape.text_vocab])
+    la = l0[shape.text_vocab:].reshape(16, -1)
+    assert all(col[0, r] == oracle.argmax_f32(la[r - 1]) for r in range(1, 9))

@@ -47,7 +47,7 @@ MUTANTS = {
     "penalty_per_occurrence": ("    if (seen) continue;\n", "    (void)seen;\n"),
     "top_k_off_by_one": ("tk = srt[top_k - 1];", "tk = srt[top_k];"),
     "nucleus_drops_the_cut": ("        tp = val;\n", "        tp = start > 0 ? srt[start - 1] : val;\n"),
-    "cdf_not_strict": ("    if (run > target) {", "    if (run >= target) {"),
+    "cdf_not_strict": ("    if (run > target) return i;", "    if (run >= target) return i;"),
     "cdf_ignores_kept_set": ("    if (!(e[i] > 0.f && e[i] >= tp)) continue;\n", "    if (!(e[i] > 0.f)) continue;\n"),
 }
 

@@ -140,6 +140,6 @@ def test_sample_ties_at_the_cuts_are_kept():
 
 def test_sample_without_finite_logits_returns_zero():
     bad = np.array([np.nan, -np.inf, np.nan], np.float32)
-    assert oracle.sample(bad, 0.5) == (0, False, 0)
+    assert oracle.sample(bad, 0.5) == (0, {0}, 0)
     mixed = np.array([np.nan, -np.inf, 0.5, np.inf], np.float32)
     assert oracle.sample(mixed, 0.9)[0] == 2                 # only the finite logit counts
