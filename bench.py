@@ -474,6 +474,14 @@ def main():
               "p50_ms": float(np.percentile(per1, 50)), "p99_ms": float(np.percentile(per1, 99)),
               "positions": [max(3, a.warmup), max(3, a.warmup) + a.b1_steps]}
         e1.close_engine()
+        if a.skip_user_steps_steps > 0:   # the low-B variant beside the literal 16 steps
+            e1 = pp.Engine(shape, 1, w_dev, flags=a.engine_flags | pp.PP_FLAG_SKIP_USER_STEPS)
+            e1.open(0)
+            ms1, per1 = time_ticks(e1, 1, shape, a.b1_steps, max(3, a.warmup), 700)
+            b1["skip_user_steps"] = {"session_frames_s": a.b1_steps / (ms1 / 1000.0),
+                                     "p50_ms": float(np.percentile(per1, 50)),
+                                     "p99_ms": float(np.percentile(per1, 99))}
+            e1.close_engine()
 
     # -- CPU oracle baseline (rank 0, N=1 only) -------------------------------------------
     cpu = None

@@ -305,7 +305,12 @@ class Driver:
         except Exception:
             pass
 
-    def open(self, voice=None, persona=None, silence=None, silence_ticks=0, engine=None):
+    def open(self, voice=None, persona=None, silence=None, silence_ticks=0, engine=None,
+             sampling=None):
+        """Admit a session (lowest free slot) and open it on `engine`; `sampling` (a
+        pp_sampling) sets its sampling parameters there."""
+        if sampling is not None and engine is None:
+            raise ValueError("sampling parameters live on the engine: pass engine=")
         keep = []
         def arr(a):
             if a is None:
@@ -320,6 +325,8 @@ class Driver:
         slot = ctypes.c_int(-1)
         _check("pp_driver_open", lib().pp_driver_open(self.h, engine.h if engine else None,
                                                       ctypes.byref(pr), ctypes.byref(slot)))
+        if sampling is not None:
+            engine.set_sampling(slot.value, sampling)
         return slot.value
 
     def close(self, slot, engine=None):

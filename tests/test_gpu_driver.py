@@ -109,3 +109,42 @@ def test_driver_sessions_match_the_oracle():
         for f in range(len(cols) - 1):
             assert outs[f + 1][0] == cols[f][0] and outs[f + 1][1] == cols[f][1]
             assert np.array_equal(outs[f + 1][2:], cols[f + 1][2:9])
+
+
+def test_driver_open_sets_sampling_on_the_engine():
+    """Driver.open(sampling=...) samples that session; a later admission into the same
+    slot starts greedy again."""
+    import full_duplex_speech_lockstep_gb300 as pp
+    shape = synth.TINY
+    w_host = synth.make_weights_host(shape, 3)
+    eng = pp.Engine(shape, 2, device_weights(w_host))
+    drv = pp.Driver(2, shape.text_vocab, shape.audio_card)
+    S = pp.sampling(text_temperature=1.5, audio_temperature=1.5, seed=9)
+    slot = drv.open(engine=eng, sampling=S)
+    with pytest.raises(ValueError):
+        drv.open(sampling=S)                       # parameters need the engine
+    import torch
+    lg = torch.empty((2, eng.logits_ld), dtype=torch.float32, device="cuda")
+    differs = 0
+    for t in range(6):
+        u = synth.uniform_i32(2 * 8, 21, 200 + t, 0, shape.audio_card).reshape(2, 8)
+        prev, user, mask, forced = drv.prepare(u)
+        col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda(),
+                       torch.from_numpy(mask).cuda(), torch.from_numpy(forced).cuda(),
+                       logits=lg).cpu().numpy()
+        drv.absorb(u, col)
+        l0 = lg[slot].cpu().numpy()
+        la = l0[shape.text_vocab:].reshape(16, -1)
+        differs += sum(int(col[slot, r] != oracle.argmax_f32(la[r - 1]))
+                       for r in range(1, 9) if not mask[slot, r])
+    assert differs > 10                            # hot sampling leaves greedy often
+    drv.close(slot, engine=eng)
+    assert drv.open(engine=eng) == slot            # recycled: greedy again
+    u = synth.uniform_i32(2 * 8, 21, 300, 0, shape.audio_card).reshape(2, 8)
+    prev, user, mask, forced = drv.prepare(u)
+    col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda(),
+                   torch.from_numpy(mask).cuda(), torch.from_numpy(forced).cuda(),
+                   logits=lg).cpu().numpy()
+    l0 = lg[slot].cpu().numpy()
+    assert col[slot, 0] == oracle.argmax_f32(l0[:shape.text_vocab])
+

@@ -260,3 +260,35 @@ def test_tick_sampling_is_slot_independent_and_reset_on_open():
     assert col[0, 0] == oracle.argmax_f32(l0[:shape.text_vocab])
     la = l0[shape.text_vocab:].reshape(16, -1)
     assert all(col[0, r] == oracle.argmax_f32(la[r - 1]) for r in range(1, 9))
+
+
+def test_sampling_state_is_sliced_per_slot_group():
+    """With the batch split into two slot groups (PP_FLAG_TWO_GROUPS), a sampled session
+    in group 1 (slot 12) gives the same columns as in group 0 (slot 2) of a one-group
+    engine: the per-slot parameters and text history are addressed per group."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    shape = synth.TINY
+    w_dev = device_weights(synth.make_weights_host(shape, 5))
+    P = pp.sampling(text_temperature=1.1, text_top_k=30, repetition_penalty=1.4,
+                    penalty_window=5, audio_temperature=0.7, audio_top_p=0.9, seed=77)
+    B, T = 16, 8
+
+    def run(flags, slot):
+        eng = pp.Engine(shape, B, w_dev, flags=flags)
+        eng.open(slot)
+        eng.set_sampling(slot, P)
+        prev = np.stack([initial_column(shape)] * B)
+        cols = []
+        for t in range(T):
+            user = np.tile(synth.uniform_i32(8, 61, 600 + t, 0, shape.audio_card), (B, 1))
+            col = eng.step(torch.from_numpy(prev).cuda(), torch.from_numpy(user).cuda()).cpu().numpy()
+            cols.append(col[slot].copy())
+            prev = np.where(col < 0, initial_column(shape)[None, :], col).astype(np.int32)
+        eng.close_engine()
+        return np.stack(cols)
+
+    a = run(0, 2)
+    b = run(pp.PP_FLAG_TWO_GROUPS, 12)
+    assert np.array_equal(a, b)
+
