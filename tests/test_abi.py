@@ -101,3 +101,31 @@ def test_sampling_rejects_bad_arguments_without_touching_the_gpu():
     assert call(R=0.0) == pp.PP_EINVAL
     assert lib.pp_sample(None, 64, 0, 64, 0.7, 0, 0.9, 1.0, ctypes.c_void_p(16), 300, None,
                          None, None, None, None) == pp.PP_EINVAL   # history without counts
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """The ctypes structures mirror pp.h field for field: offsets and sizes from a C
+    program compiled against the header equal the binding's."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    structs = {"pp_config": pp.pp_config, "pp_sampling": pp.pp_sampling,
+               "pp_prompt": pp.pp_prompt, "pp_weights": pp.pp_weights}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "pp.h"', 'int main(void) {']
+    for name, cls in structs.items():
+        lines.append('  printf("%s size %%zu\\n", sizeof(%s));' % (name, name))
+        for f in cls._fields_:
+            lines.append('  printf("%s %s %%zu\\n", offsetof(%s, %s));' % (name, f[0], name, f[0]))
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.check_call(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for f in cls._fields_:
+            assert got[(name, f[0])] == getattr(cls, f[0]).offset, (name, f[0])
