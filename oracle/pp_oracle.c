@@ -3,7 +3,8 @@
  * loaded by tests, the smoke check and the bench's CPU-baseline leg, never by the
  * product.  See pp_oracle.h for the arithmetic contract and the pages it follows.
  *
- * Style: plain loops in the order the definitions state them, fp64 throughout,
+ * Style: plain loops in the order the definitions state them, fp64 throughout (the
+ * sampling variants' fp32 decision steps excepted, see there),
  * OpenMP only across independent output rows of a matrix-vector product (each row's
  * dot product is one sequential loop), so results do not depend on the thread count.
  */

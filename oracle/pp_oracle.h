@@ -12,7 +12,8 @@
  * nearest even), because the cache is a bf16 tensor (the full-window stress case fills
  * it with random bf16 values).  Logits are rounded to fp32 and the greedy decision
  * is taken on those fp32 values (the GPU kernel's precision), lowest index on ties,
- * NaN never chosen.
+ * NaN never chosen.  The sampling variants likewise take their decision steps (penalty,
+ * temperature, expf) in fp32 and accumulate probability masses in fp64.
  *
  * Sources (page title, section):
  *  - vllm-omni recipes/NVIDIA/PersonaPlex.md, "Architecture": temporal 4096-d / 32
