@@ -1,6 +1,7 @@
 // k_tick.cu - the light kernels of one lockstep tick: control + 17-table embedding
-// sum + RoPE angle table, RMSNorm, RoPE + ring-KV write, the fused greedy heads, the
-// depformer step attention and the end-of-tick bookkeeping.
+// sum + RoPE angle table, RMSNorm, RoPE + ring-KV write, the token decisions (greedy,
+// forced, or sampled per session), the depformer step attention and the end-of-tick
+// bookkeeping.
 #include <math.h>
 
 #include "pp_internal.cuh"
