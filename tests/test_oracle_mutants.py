@@ -1,6 +1,7 @@
-"""The pins must catch plausible mistakes: each case below plants one mistake in a
-temporary copy of the oracle source (never in the committed file), rebuilds it, runs
-the pin suite against the copy in a subprocess and expects a failure."""
+"""The pins must catch plausible mistakes: each case below plants one mistake (one or
+more edits of the same slip) in a temporary copy of the oracle source (never in the
+committed file), rebuilds it, runs the pin suite against the copy in a subprocess and
+expects a failure."""
 import os
 import shutil
 import subprocess
@@ -49,6 +50,28 @@ MUTANTS = {
     "nucleus_drops_the_cut": ("        tp = val;\n", "        tp = start > 0 ? srt[start - 1] : val;\n"),
     "cdf_not_strict": ("    if (run > target) return i;", "    if (run >= target) return i;"),
     "cdf_ignores_kept_set": ("    if (!(e[i] > 0.f && e[i] >= tp)) continue;\n", "    if (!(e[i] > 0.f)) continue;\n"),
+    # the depformer's own MLP, step attention and per-frame cache
+    "dep_gate_up_swapped": ("h[i] = silu(gu[i]) * gu[Fd + i];", "h[i] = gu[i] * silu(gu[Fd + i]);"),
+    "dep_no_score_scale": ("sc[j] = dot / sqrt((double)Dhd);", "sc[j] = dot;"),
+    "dep_scale_by_width": ("sc[j] = dot / sqrt((double)Dhd);", "sc[j] = dot / sqrt((double)dd);"),
+    "dep_mlp_norm_wrong_alpha": ("ora_rmsnorm(y, w->dep_mlp_alpha + (int64_t)l * dd, dd, s->eps, n);",
+                                 "ora_rmsnorm(y, w->dep_attn_alpha + (int64_t)l * dd, dd, s->eps, n);"),
+    # the cache is made once (large enough for every test shape), never cleared, and
+    # read over all of its 16 entries
+    "dep_cache_carried_across_frames": [
+        ("  double* kc = (double*)calloc((size_t)Ld * nq * dd, sizeof(double));\n"
+         "  double* vc = (double*)calloc((size_t)Ld * nq * dd, sizeof(double));\n",
+         "  static double* kc = 0;\n  static double* vc = 0;\n"
+         "  if (!kc) kc = (double*)calloc((size_t)8 * 16 * 4096, sizeof(double));\n"
+         "  if (!vc) vc = (double*)calloc((size_t)8 * 16 * 4096, sizeof(double));\n"),
+        ("free(lg); free(lf); free(kc); free(vc); free(sc);", "free(lg); free(lf); free(sc);"),
+        ("for (int j = 0; j <= k; ++j) {\n          const double* kj",
+         "for (int j = 0; j < nq; ++j) {\n          const double* kj"),
+        ("for (int j = 0; j <= k; ++j) { sc[j] = exp(sc[j] - m); lsum += sc[j]; }",
+         "for (int j = 0; j < nq; ++j) { sc[j] = exp(sc[j] - m); lsum += sc[j]; }"),
+        ("for (int j = 0; j <= k; ++j)\n            acc += sc[j]",
+         "for (int j = 0; j < nq; ++j)\n            acc += sc[j]"),
+    ],
 }
 
 # mistakes in the sampling variants, caught by their own pin file
@@ -60,11 +83,15 @@ SAMPLING = {"philox_key_bump_swapped", "philox_products_swapped", "uniform_low_b
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, tmp_path):
-    old, new = MUTANTS[name]
+    edits = MUTANTS[name]
+    if isinstance(edits, tuple):
+        edits = [edits]
     src = open(SRC).read()
-    assert src.count(old) == 1, "mutation anchor not found: %s" % name
+    for old, new in edits:
+        assert src.count(old) == 1, "mutation anchor not found: %s" % name
+        src = src.replace(old, new)
     shutil.copy(os.path.join(ROOT, "oracle", "pp_oracle.h"), tmp_path / "pp_oracle.h")
-    (tmp_path / "pp_oracle.c").write_text(src.replace(old, new))
+    (tmp_path / "pp_oracle.c").write_text(src)
     so = str(tmp_path / "libmutant.so")
     subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
                            "-std=c11", str(tmp_path / "pp_oracle.c"), "-o", so, "-lm"])

@@ -437,6 +437,136 @@ def test_depformer_inproj_and_step_attention():
         assert np.all(logits[k, dd:] == 0)
 
 
+def _dep_identity_heads(s):
+    heads = np.zeros((s.n_q, s.audio_card, s.dep_d), np.float32)
+    heads[:, np.arange(s.dep_d), np.arange(s.dep_d)] = 1
+    return bf16_exact(heads)
+
+
+def test_depformer_mlp_gate_up_down_wiring():
+    """Depformer attention off (W_qkv = W_o = 0), token tables 0, P_k selects z entries,
+    [g; u] = [P_g; P_u] n with n = RMSNorm(e_k) * mlp_alpha (random), W_down selects:
+    the step-k state is e_k + (silu(g) * u)[src_d], read through identity heads."""
+    s = _one_layer(TINY, 8)
+    d, dd, Fd = s.d, s.dep_d, s.dep_ffn
+    w = synth.make_weights_host(s, 8, alpha="random")
+    w["dep_emb_text"], w["dep_emb_audio"] = _zero(w["dep_emb_text"]), _zero(w["dep_emb_audio"])
+    srcs = [permutation(d, 60 + k)[:dd] for k in range(16)]
+    w["dep_inproj"] = bf16_exact(np.stack([perm_matrix(dd, d, sk) for sk in srcs]))
+    w["dep_wqkv"], w["dep_wo"] = _zero(w["dep_wqkv"]), _zero(w["dep_wo"])
+    rng = np.random.default_rng(61)
+    src_g, src_u = rng.integers(0, dd, Fd), rng.integers(0, dd, Fd)
+    src_d = permutation(Fd, 62)[:dd]
+    w["dep_wgu"] = bf16_exact(np.concatenate([perm_matrix(Fd, dd, src_g),
+                                              perm_matrix(Fd, dd, src_u)])[None])
+    w["dep_wdown"] = bf16_exact(perm_matrix(dd, Fd, src_d)[None])
+    w["dep_heads"] = _dep_identity_heads(s)
+    o = oracle.Oracle(s, w)
+    z = np.random.default_rng(63).standard_normal(d) * 2.0
+    _, logits = o.depformer(z, 5, np.zeros(8, np.int32))
+    for k in range(16):
+        e = z[srcs[k]]
+        n = _norm(e, w["dep_mlp_alpha"][0], s.eps)
+        g, u = n[src_g], n[src_u]
+        h = g / (1 + np.exp(-g)) * u
+        ref = _norm(e + h[src_d], w["dep_out_alpha"], s.eps)
+        assert np.allclose(logits[k, :dd], ref, rtol=2e-6, atol=1e-7), k
+
+
+def _brute_depformer(s, w, z, tokens):
+    """Numpy model of one frame's depformer as a single teacher-forced pass over all 16
+    codebook positions at once: every position's input is known in advance (tokens[k]
+    feeds step k), and causality is a -inf mask on the score matrix instead of a cache
+    that grows step by step.  Returns the 16 heads' logits [16, Va] (fp64)."""
+    dd, Hd, Fd, nq = s.dep_d, s.dep_heads, s.dep_ffn, s.n_q
+    Dhd = dd // Hd
+    X = np.empty((nq, dd))
+    for k in range(nq):
+        table = (bf16_to_f64(w["dep_emb_text"][tokens[0]]) if k == 0
+                 else bf16_to_f64(w["dep_emb_audio"][k - 1, tokens[k]]))
+        X[k] = bf16_to_f64(w["dep_inproj"][k]) @ z + table
+
+    def norm_rows(A, alpha):
+        return A / np.sqrt(np.mean(A * A, axis=1, keepdims=True) + s.eps) * alpha.astype(np.float64)
+
+    mask = np.triu(np.full((nq, nq), -np.inf), 1)          # position i sees j <= i
+    for l in range(s.dep_layers):
+        N = norm_rows(X, w["dep_attn_alpha"][l])
+        QKV = N @ bf16_to_f64(w["dep_wqkv"][l]).T
+        Q, K, V = (QKV[:, i * dd:(i + 1) * dd].reshape(nq, Hd, Dhd) for i in range(3))
+        S = np.einsum("ihc,jhc->hij", Q, K) / np.sqrt(Dhd) + mask
+        P = scipy.special.softmax(S, axis=-1)
+        O = np.einsum("hij,jhc->ihc", P, V).reshape(nq, dd)
+        X = X + O @ bf16_to_f64(w["dep_wo"][l]).T
+        N = norm_rows(X, w["dep_mlp_alpha"][l])
+        GU = N @ bf16_to_f64(w["dep_wgu"][l]).T
+        G, U = GU[:, :Fd], GU[:, Fd:]
+        X = X + (scipy.special.expit(G) * G * U) @ bf16_to_f64(w["dep_wdown"][l]).T
+    Zd = norm_rows(X, w["dep_out_alpha"])
+    return np.stack([bf16_to_f64(w["dep_heads"][k]) @ Zd[k] for k in range(nq)])
+
+
+def _scale_rows(wt, rows, factor):
+    """bf16 weights with the given rows of every layer multiplied by a power of two."""
+    v = bf16_to_f64(wt).copy()
+    v[:, rows] *= factor
+    return bf16_exact(v.astype(np.float32))
+
+
+def test_depformer_equals_teacher_forced_causal_pass():
+    """Random depformer weights (two layers, q and k rows scaled so the step attention is
+    far from uniform), every agent row forced: the oracle's step-by-step decode with a
+    per-frame cache equals one masked pass over the 16 known positions."""
+    s = dataclasses.replace(TINY, dep_layers=2)
+    dd = s.dep_d
+    w = synth.make_weights_host(s, 9, alpha="random")
+    w["dep_wqkv"] = _scale_rows(w["dep_wqkv"], slice(0, 2 * dd), 4.0)
+    o = oracle.Oracle(s, w)
+    rng = np.random.default_rng(64)
+    for trial in range(3):
+        z = rng.standard_normal(s.d)
+        text = int(rng.integers(0, s.text_vocab + 1))
+        agent = rng.integers(0, s.audio_card + 1, 8).astype(np.int32)
+        user = rng.integers(0, s.audio_card, 8).astype(np.int32)
+        fm = np.zeros(17, np.uint8)
+        ft = np.zeros(17, np.int32)
+        fm[1:9], ft[1:9] = 1, agent
+        col, logits = o.depformer(z, text, user, fm, ft)
+        assert np.array_equal(col[1:9], agent) and np.array_equal(col[9:], user)
+        tokens = np.concatenate([[text], agent, user[:7]])
+        ref = _brute_depformer(s, w, z, tokens)
+        scale = np.abs(ref).max()
+        assert np.allclose(logits, ref, rtol=1e-6, atol=1e-6 * scale), trial
+
+
+def test_depformer_resets_every_frame():
+    """The depformer's cache holds the current frame's steps only: each frame's rows 1..16
+    and audio logits, taken in sequence through whole ticks, are bitwise those of the
+    same frame's depformer run alone from its (z, text token, user codes), in order and
+    in a shuffled order."""
+    s = TINY
+    w = synth.make_weights_host(s, 10, alpha="random")
+    w["dep_wqkv"] = _scale_rows(w["dep_wqkv"], slice(0, 2 * s.dep_d), 4.0)
+    o = oracle.Oracle(s, w)
+    T = 6
+    cols = _columns(s, T, 10)
+    users = synth.uniform_i32(T * 8, 10, 13, 0, s.audio_card).reshape(T, 8)
+    seq = o.new_session()
+    rep = o.new_session()          # the same frames again, to read each frame's z
+    frames = []
+    for t in range(T):
+        col, _, la = o.step(seq, cols[t], users[t])
+        z = o.temporal(rep, cols[t])
+        rep.c.pos += 1
+        frames.append((z, int(col[0]), users[t], col, la))
+    for order in (range(T), np.random.default_rng(11).permutation(T)):
+        for t in order:
+            z, text, user, col, la = frames[t]
+            c2, l2 = o.depformer(z, text, user)
+            assert np.array_equal(c2[1:], col[1:]), t
+            assert np.array_equal(l2, la), t
+
+
 # ---- Mimi RVQ dequantisation -----------------------------------------------------------
 
 def _rvq_books(n_books=8, card=64, dim=16, seed=3):
