@@ -33,9 +33,9 @@ UNIT = "session-frames/s"
 SEED = 5
 HBM_NOMINAL_GBS = 8000.0
 
-# DRAM traffic of the attention kernel from one ncu capture (profiles/
-# k_attn_tc_b8_fullshape_2layers.md): dram__bytes_read + dram__bytes_write of one launch
-# at B=8 with a full 3000-position ring, per (slot, valid position).  Traffic grows in
+# DRAM traffic of the attention kernel from one ncu capture (the --set full capture of one
+# launch at B=8 with a full 3000-position ring, two temporal layers): dram__bytes_read +
+# dram__bytes_write of that launch per (slot, valid position).  Traffic grows in
 # proportion to the slots, so a full launch's traffic is this times slots x positions.
 # Valid only while k_attn_tc.cu is the source that was captured (its hash below).
 ATTN_TRAFFIC = {"bytes_per_slot_position": (394.677248e6 + 5.22368e6) / (8 * 3000),

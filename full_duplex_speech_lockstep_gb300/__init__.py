@@ -41,7 +41,7 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
            "pp_ring_attention_noalloc", "pp_rvq_dequantize", "pp_driver_create",
            "pp_driver_destroy", "pp_driver_open", "pp_driver_close", "pp_driver_phase",
            "pp_driver_prepare", "pp_driver_absorb", "pp_driver_tick", "pp_session_sampling",
-           "pp_sample"]
+           "pp_sample", "pp_test_faults"]
 
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
@@ -121,13 +121,15 @@ def lib():
         L.pp_status.restype = I
         L.pp_step_kernel_count.argtypes = [P]
         L.pp_step_kernel_count.restype = I
+        L.pp_test_faults.argtypes = [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P]
+        L.pp_test_faults.restype = I
         L.pp_profile_step.argtypes = [P] * 10
         L.pp_profile_step.restype = I
         L.pp_ring_attention_scratch_bytes.argtypes = [I, I, I, I]
         L.pp_ring_attention_scratch_bytes.restype = ctypes.c_size_t
-        L.pp_ring_attention.argtypes = [P, P, P, I64, P, I, I, I, I, P, P, ctypes.c_size_t, P]
+        L.pp_ring_attention.argtypes = [P, P, P, I64, P, I, I, I, I, P, P, P, ctypes.c_size_t, P]
         L.pp_ring_attention.restype = I
-        L.pp_ring_attention_noalloc.argtypes = [P, P, P, I64, P, I, I, I, I, P, P]
+        L.pp_ring_attention_noalloc.argtypes = [P, P, P, I64, P, I, I, I, I, P, P, P]
         L.pp_ring_attention_noalloc.restype = I
         L.pp_rvq_dequantize.argtypes = [P, I, I, I, P, I, I, P, P, P]
         L.pp_rvq_dequantize.restype = I
@@ -245,6 +247,15 @@ def pp_step_kernel_count(h):
     return lib().pp_step_kernel_count(h)
 
 
+PP_TEST_UMMA, PP_TEST_ATTN = 0x1, 0x2
+
+
+def pp_test_faults(h, wait_polls, withhold, kinds, stream):
+    """Failure-detection tests only: lower the bounded waits' poll budget and have
+    producers of the named kernel families withhold copies (0, 0, 0 resets)."""
+    return _check("pp_test_faults", lib().pp_test_faults(h, wait_polls, withhold, kinds, stream))
+
+
 def pp_profile_step(h, prev_column, user_codes, force_mask, forced_tokens, column, logits,
                     stream, kind_ms, kind_launches):
     """kind_ms: ctypes double array, kind_launches: ctypes int64 array (accumulated)."""
@@ -260,18 +271,18 @@ def pp_ring_attention_scratch_bytes(B, H, head_dim, window):
     return n
 
 
-def pp_ring_attention(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, scratch,
-                      scratch_bytes, stream):
+def pp_ring_attention(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, status,
+                      scratch, scratch_bytes, stream):
     return _check("pp_ring_attention", lib().pp_ring_attention(
-        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, scratch, scratch_bytes,
-        stream))
+        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, status, scratch,
+        scratch_bytes, stream))
 
 
 def pp_ring_attention_noalloc(q, k, v, slot_stride, n_valid, B, H, head_dim, window, out,
-                              stream):
+                              status, stream):
     """pp_ring_attention with the library's built-in scratch (no allocation)."""
     return _check("pp_ring_attention_noalloc", lib().pp_ring_attention_noalloc(
-        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, stream))
+        q, k, v, slot_stride, n_valid, B, H, head_dim, window, out, status, stream))
 
 
 PP_DRV_FREE, PP_DRV_VOICE, PP_DRV_SILENCE, PP_DRV_PERSONA, PP_DRV_LIVE = 0, 1, 2, 3, 4
@@ -462,6 +473,9 @@ class Engine:
 
     def status(self):
         return pp_status(self.h, self._stream())
+
+    def test_faults(self, wait_polls=0, withhold=0, kinds=0):
+        pp_test_faults(self.h, wait_polls, withhold, kinds, self._stream())
 
     def step(self, prev_column, user_codes, force_mask=None, forced=None, logits=None,
              out=None):

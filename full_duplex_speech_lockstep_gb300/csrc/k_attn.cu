@@ -163,12 +163,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
   if (warp == kProducerWarp) {
     // ---- producer -----------------------------------------------------------------
     if (lane == 0) {
+      int32_t armed, kinds;
+      read_withhold(a.test_ctl, armed, kinds);
       int v = 0;
       for (int u = u0; u < u1; ++u) {
         const Unit t = decode_unit(a, u);
         if (t.nk == 0) continue;
         const int st = v % S;
-        if (v >= S && !mbar_wait(bar(2 * S + st), ((v / S) - 1) & 1)) raise_timeout(a, s_abort);
+        if (v >= S && !mbar_wait(bar(2 * S + st), ((v / S) - 1) & 1, a.test_ctl))
+          raise_timeout(a, s_abort);
         if (*s_abort) break;
         uint8_t* sk = smem + st * C::kStageBytes;
         const size_t off = (size_t)t.s * a.slot_stride + t.h * blk + (size_t)t.c * kAttnChunk * DH;
@@ -177,14 +180,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
         bulk_load(smem_u32(sk), a.k + off, bytes, bar(st));
         bulk_load(smem_u32(sk + 2 * C::kKVBytes), a.q + (size_t)t.s * a.q_ld + t.h * DH, DH * 4,
                   bar(st));
-        mbar_expect_tx(bar(S + st), bytes);
-        bulk_load(smem_u32(sk + C::kKVBytes), a.v + off, bytes, bar(S + st));
+        // a failure-detection test may have this producer withhold its first V tile:
+        // that stage never completes and the consumers' bounded waits run out
+        if (!(v == 0 && take_withhold(a.test_ctl, armed, kinds, PP_TEST_ATTN))) {
+          mbar_expect_tx(bar(S + st), bytes);
+          bulk_load(smem_u32(sk + C::kKVBytes), a.v + off, bytes, bar(S + st));
+        }
         ++v;
       }
       // every copy this CTA issued lands before the CTA may exit (bounded waits)
       for (int i = v > S ? v - S : 0; i < v; ++i) {
-        mbar_wait(bar(i % S), (i / S) & 1);
-        mbar_wait(bar(S + i % S), (i / S) & 1);
+        mbar_wait(bar(i % S), (i / S) & 1, a.test_ctl);
+        mbar_wait(bar(S + i % S), (i / S) & 1, a.test_ctl);
       }
     }
     return;
@@ -233,7 +240,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
       const int ps = v % kPartSlots;
       const uint32_t ph = (v / kPartSlots) & 1;
       ++v;
-      if (!*s_abort && !mbar_wait(bar(3 * S + ps), ph)) raise_timeout(a, s_abort);
+      if (!*s_abort && !mbar_wait(bar(3 * S + ps), ph, a.test_ctl)) raise_timeout(a, s_abort);
       const float* slot = s_slot + ps * (kConsumerWarps * C::kWarpPart);
       float mw[kConsumerWarps];
       float M = -INFINITY;
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
     const float* qs = reinterpret_cast<const float*>(sk + 2 * C::kKVBytes);
     const int kcount = max(0, min(kKeysPerWarp, t.nk - key0));
 
-    if (!*s_abort && !mbar_wait(bar(st), ph)) raise_timeout(a, s_abort);
+    if (!*s_abort && !mbar_wait(bar(st), ph, a.test_ctl)) raise_timeout(a, s_abort);
     // scores: lane (g, qd) holds pieces (j ^ par) * 4 + qd of the query and of its key
     float q[LOADS][8];
 #pragma unroll
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
-    if (!*s_abort && !mbar_wait(bar(S + st), ph)) raise_timeout(a, s_abort);
+    if (!*s_abort && !mbar_wait(bar(S + st), ph, a.test_ctl)) raise_timeout(a, s_abort);
     if (kcount > 0) {   // warp-uniform
 #pragma unroll
       for (int it = 0; it < ITER; ++it) {
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attn(AttnArgs a, int units)
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     // warp partial into the unit's slot
-    if (reuse_slot && !*s_abort && !mbar_wait(bar(3 * S + kPartSlots + ps), pph))
+    if (reuse_slot && !*s_abort && !mbar_wait(bar(3 * S + kPartSlots + ps), pph, a.test_ctl))
       raise_timeout(a, s_abort);
     float* wp = s_slot + ps * (kConsumerWarps * C::kWarpPart) + warp * C::kWarpPart;
     if (lane == 0) { wp[0] = m; wp[1] = l; }
@@ -428,6 +435,7 @@ cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, con
   a.part = b.attn_part;
   a.count = b.attn_count;
   a.status = b.status;
+  a.test_ctl = b.test_ctl;
   a.q_op = b.q_op;
   // the K/V maps span every layer's ring: slot coordinate = layer * B + slot
   return launch_attn_args(a, D.B, D.Dh, maps, layer * D.B, s);

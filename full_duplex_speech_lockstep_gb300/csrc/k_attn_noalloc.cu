@@ -28,8 +28,12 @@ constexpr size_t kNoAllocPartBytes =
 constexpr size_t kNoAllocCountBytes = (size_t)kNoAllocMaxPairs * sizeof(uint32_t);
 constexpr size_t kNoAllocQopBytes = (size_t)kNoAllocMaxPairs * 2 * kNoAllocMaxHeadDim * 2;
 constexpr size_t kNoAllocBytes = kNoAllocPartBytes + kNoAllocCountBytes + kNoAllocQopBytes;
+// 2048 pairs x 3264 floats of partials (25.5 MiB) + 8 KiB of tickets + 1 MiB of query
+// operand: the figure the header states
+static_assert(kNoAllocBytes == 27795456, "the documented size of the built-in scratch");
 
-// Every GPU that loads the library holds this array (about 25.4 MiB) until exit.
+// Every GPU that loads the library holds this array (27,795,456 bytes, about 26.5 MiB)
+// until exit.
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
@@ -62,7 +66,7 @@ using namespace pp;
 extern "C" int pp_ring_attention_noalloc(const float* q, const uint16_t* k, const uint16_t* v,
                                          int64_t slot_stride, const int32_t* n_valid, int B,
                                          int H, int head_dim, int window, float* out,
-                                         void* stream) {
+                                         uint32_t* status, void* stream) {
   if (B < 1 || H < 1 || window < 1) return PP_EINVAL;
   if (head_dim != 32 && head_dim != 64 && head_dim != 128) return PP_EINVAL;
   if ((int64_t)B * H > kNoAllocMaxPairs || window > kNoAllocMaxWindow ||
@@ -90,6 +94,7 @@ extern "C" int pp_ring_attention_noalloc(const float* q, const uint16_t* k, cons
   a.out = out;
   a.out_ld = H * head_dim;
   a.op = nullptr;
+  a.status = status;
   char* sp = reinterpret_cast<char*>(base);
   a.part = reinterpret_cast<float*>(sp);
   a.count = reinterpret_cast<uint32_t*>(sp + kNoAllocPartBytes);

@@ -95,7 +95,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int col) {
 __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity, const AttnArgs& a,
                                              volatile int* abort_flag) {
   if (*abort_flag) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity, a.test_ctl)) return true;
   raise_timeout(a, abort_flag);
   return false;
 }
@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int vk = 0, vv = 0;
       int uk = next_valid(u0), uv = uk;
-      uint32_t idle = 0;
+      uint32_t idle = 0, idle_limit = 4 * kWaitLimit;
+      int32_t armed, kinds;
+      read_withhold(a.test_ctl, armed, kinds);
       while ((uk < u1 || uv < u1) && !*abort_flag) {
         bool progressed = false;
         if (uk < u1 && (vk < kKStages || mbar_test(B32(ctl->kempty[vk % kKStages]),
@@ -184,24 +186,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vb = smem_u32(smem + kVOff + (vv % kVStages) * kKVBytes);
           const uint32_t full = B32(ctl->vfull[vv % kVStages]);
           const int row = t.c * kAttnChunk, sc = slot_base + t.s;
-          mbar_expect_tx(full, kKVBytes);
-          tma_load_4d(vb, &mapV, 0, row, t.h, sc, full);
-          tma_load_4d(vb + kBoxBytes, &mapV, 64, row, t.h, sc, full);
+          // a failure-detection test may have this producer withhold its first V tile:
+          // that stage never completes and the MMA issuer's bounded polling runs out
+          if (!(vv == 0 && take_withhold(a.test_ctl, armed, kinds, PP_TEST_ATTN))) {
+            mbar_expect_tx(full, kKVBytes);
+            tma_load_4d(vb, &mapV, 0, row, t.h, sc, full);
+            tma_load_4d(vb + kBoxBytes, &mapV, 64, row, t.h, sc, full);
+          }
           ++vv;
           uv = next_valid(uv + 1);
           progressed = true;
         }
         if (progressed) {
           idle = 0;
-        } else if (++idle > 4 * kWaitLimit) {
+        } else if (++idle > idle_limit) {
           raise_timeout(a, abort_flag);
+        } else if (idle == kWaitFastPolls) {
+          idle_limit = 4 * wait_budget(a.test_ctl);
         }
       }
       // every copy this CTA issued lands before the CTA may exit (bounded waits)
       for (int i = vk > kKStages ? vk - kKStages : 0; i < vk; ++i)
-        mbar_wait(B32(ctl->kfull[i % kKStages]), (i / kKStages) & 1);
+        mbar_wait(B32(ctl->kfull[i % kKStages]), (i / kKStages) & 1, a.test_ctl);
       for (int i = vv > kVStages ? vv - kVStages : 0; i < vv; ++i)
-        mbar_wait(B32(ctl->vfull[i % kVStages]), (i / kVStages) & 1);
+        mbar_wait(B32(ctl->vfull[i % kVStages]), (i / kVStages) & 1, a.test_ctl);
     }
   } else if (warp == 1) {
     // ---- MMA issuer ---------------------------------------------------------------------
@@ -213,7 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // neither waits behind the other; a bounded number of idle polls raises the timeout.
       int vq = 0, vp = 0;
       int uq = next_valid(u0);
-      uint32_t idle = 0;
+      uint32_t idle = 0, idle_limit = 4 * kWaitLimit;
+      // barrier and parity of the most recent commit: MMAs complete in issue order, so
+      // once it has arrived every MMA of this CTA is done
+      uint32_t last_bar = 0, last_par = 0;
       while ((uq < u1 || vp < vq) && !*abort_flag) {
         bool progressed = false;
         if (uq < u1 && vq < vp + kBufs) {
@@ -232,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(B32(ctl->sfull[i]));
             umma_commit(B32(ctl->kempty[ks]));
+            last_bar = B32(ctl->sfull[i]);
+            last_par = (vq / kBufs) & 1;
             ++vq;
             uq = next_valid(uq + 1);
             progressed = true;
@@ -254,18 +267,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(B32(ctl->ofull[i]));
             umma_commit(B32(ctl->vempty[vs]));
+            last_bar = B32(ctl->ofull[i]);
+            last_par = (vp / kBufs) & 1;
             ++vp;
             progressed = true;
           }
         }
         if (progressed) {
           idle = 0;
-        } else if (++idle > 4 * kWaitLimit) {
+        } else if (++idle > idle_limit) {
           raise_timeout(a, abort_flag);
+        } else if (idle == kWaitFastPolls) {
+          idle_limit = 4 * wait_budget(a.test_ctl);
         }
       }
-      // the last MMAs complete before the tensor memory is released
-      if (vp > 0) mbar_wait(B32(ctl->ofull[(vp - 1) % kBufs]), ((vp - 1) / kBufs) & 1);
+      // the last MMAs complete before the tensor memory is released (also after a
+      // timeout, when score MMAs may have been issued after the last output MMA)
+      if (vq > 0) mbar_wait(last_bar, last_par, a.test_ctl);
     }
     __syncwarp();
   } else if (warp == 2) {

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b, const float* a
     pos_s = b.pos[s];
     b.nvalid[s] = live_s ? min(pos_s + 1, D.W) : 0;
   }
+  // this slot's attention tickets start the tick at zero (the merges leave them zero; a
+  // tick whose bounded wait gave up may not have)
+  for (int h = threadIdx.x; h < D.H; h += blockDim.x) b.attn_count[(size_t)s * D.H + h] = 0u;
   __syncthreads();
   if (threadIdx.x < kRows) {
     const int r = threadIdx.x;

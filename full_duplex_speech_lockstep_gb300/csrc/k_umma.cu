@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(128, 2)
     // The weights do not depend on the previous kernel: the first stages' weight tiles
     // are requested before waiting for it (programmatic dependent launch), the
     // activation tiles after.
+    int32_t armed, kinds;
+    read_withhold(a.test_ctl, armed, kinds);   // used after the dependency wait
     const int pre = nkb < C::kStages ? nkb : C::kStages;
     for (int i = 0; i < pre; ++i) {
       uint8_t* sa = smem + i * C::kStageBytes;
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(128, 2)
     for (int i = 0; i < nkb; ++i) {
       const int s = i % C::kStages;
       if (i >= C::kStages &&
-          !mbar_wait(smem_u32(&bars[C::kStages + s]), ((i / C::kStages) - 1) & 1)) {
+          !mbar_wait(smem_u32(&bars[C::kStages + s]), ((i / C::kStages) - 1) & 1, a.test_ctl)) {
         *abort_flag = 1;
         break;
       }
@@ -160,20 +162,23 @@ __global__ void __launch_bounds__(128, 2)
         tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
         tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
       }
-      tma_load_2d(smem_u32(sb), &mapB, kx, 0, full);
+      // a failure-detection test may have this producer withhold the first activation
+      // tile: its stage never completes and the MMA issuer's bounded wait runs out
+      if (!(i == 0 && take_withhold(a.test_ctl, armed, kinds, PP_TEST_UMMA)))
+        tma_load_2d(smem_u32(sb), &mapB, kx, 0, full);
       ++issued;
     }
     if (*abort_flag) {  // drain this CTA's copies still in flight (bounded waits)
       const int inflight = issued > pre ? issued : pre;
       for (int i = 0; i < inflight; ++i)
-        mbar_wait(smem_u32(&bars[i % C::kStages]), (i / C::kStages) & 1);
+        mbar_wait(smem_u32(&bars[i % C::kStages]), (i / C::kStages) & 1, a.test_ctl);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer --------------------------------------------------------------------
     constexpr uint32_t idesc = instr_desc(128, N);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % C::kStages;
-      if (!mbar_wait(smem_u32(&bars[s]), (i / C::kStages) & 1)) {
+      if (!mbar_wait(smem_u32(&bars[s]), (i / C::kStages) & 1, a.test_ctl)) {
         *abort_flag = 1;
         break;
       }
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(128, 2)
   __syncwarp();
 
   // ---- epilogue ----------------------------------------------------------------------
-  const bool done = mbar_wait(smem_u32(&bars[2 * C::kStages]), 0);
+  const bool done = mbar_wait(smem_u32(&bars[2 * C::kStages]), 0, a.test_ctl);
   if (!done) *abort_flag = 1;
   pdl_trigger();   // main loop over: the next kernel may start launching
   __syncthreads();

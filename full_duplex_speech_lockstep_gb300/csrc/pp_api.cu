@@ -88,6 +88,7 @@ struct pp_engine {
   bool samp_dirty = false;
   std::vector<int64_t> pos;            // host mirror of each open slot's position
   std::vector<uint8_t> open;
+  int32_t test_word[4] = {0, 0, 0, 0};  // host copy of the fault-test word
 };
 
 namespace {
@@ -156,6 +157,7 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
   sh.ctl = cv.take<int32_t>(B);
   sh.ctl_pos = cv.take<int32_t>(B);
   sh.status = cv.take<uint32_t>(1);
+  sh.test_ctl = cv.take<int32_t>(4);
   sh.samp = cv.take<SampleParams>(B);
   sh.hist_len = cv.take<int32_t>(B);
   sh.hist = cv.take<int32_t>(B * kHist);
@@ -398,6 +400,7 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   a.ld_op = ld_op;
   a.Bp_out = D.Bp;
   a.status = b.status;
+  a.test_ctl = b.test_ctl;
   return launch_umma(a, g.mapA, g.mapB, s);
 }
 
@@ -1042,6 +1045,20 @@ int pp_status(pp_engine* e, void* stream, uint32_t* bits) {
 
 int pp_step_kernel_count(pp_engine* e) { return e ? e->n_kernels : PP_EINVAL; }
 
+int pp_test_faults(pp_engine* e, int32_t wait_polls, int32_t withhold, int32_t kinds,
+                   void* stream) {
+  if (!e || wait_polls < 0 || withhold < 0) return PP_EINVAL;
+  if (kinds & ~(PP_TEST_UMMA | PP_TEST_ATTN)) return PP_EINVAL;
+  e->test_word[0] = wait_polls;
+  e->test_word[1] = withhold;
+  e->test_word[2] = kinds;
+  e->test_word[3] = 0;
+  // pageable source: the runtime stages it before returning, so the word may change next
+  const cudaError_t err = cudaMemcpyAsync(e->shared.test_ctl, e->test_word, sizeof(e->test_word),
+                                          cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  return err == cudaSuccess ? PP_OK : PP_E_CUDA;
+}
+
 int pp_sample(const float* logits, int64_t ld, int rows, int n, float temperature, int top_k,
               float top_p, float penalty, const int32_t* hist, int hist_ld,
               const int32_t* hist_n, const float* uniforms, int32_t* tokens, uint32_t* status,
@@ -1087,7 +1104,8 @@ size_t pp_ring_attention_scratch_bytes(int B, int H, int head_dim, int window) {
 
 int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int64_t slot_stride,
                       const int32_t* n_valid, int B, int H, int head_dim, int window,
-                      float* out, void* scratch, size_t scratch_bytes, void* stream) {
+                      float* out, uint32_t* status, void* scratch, size_t scratch_bytes,
+                      void* stream) {
   if (!ring_attention_args_ok(B, H, head_dim, window)) return PP_EINVAL;
   if (!q || !k || !v || !n_valid || !out || !scratch || slot_stride < 0) return PP_EINVAL;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
@@ -1109,6 +1127,7 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
   a.out = out;
   a.out_ld = H * head_dim;
   a.op = nullptr;
+  a.status = status;
   char* sp = reinterpret_cast<char*>(scratch);
   a.part = reinterpret_cast<float*>(sp);
   sp += ring_attention_part_bytes(B, H, head_dim, window);

@@ -6,7 +6,7 @@
 
 namespace pp {
 
-constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up
+constexpr uint32_t kWaitLimit = 1u << 24;   // polls before a wait gives up (default)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -48,11 +48,47 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: true when the phase completed, false after kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Fault-test word of an engine (pp_test_faults): [0] poll budget of a bounded wait
+// (<= 0: kWaitLimit), [1] copies a producer still has to withhold, [2] the kernel
+// families that withhold (PP_TEST_*).  A null pointer means the defaults.
+constexpr uint32_t kWaitFastPolls = 1024;   // polls before a wait reads its budget
+
+// Poll budget of a bounded wait; the word is read only by a wait that has already
+// lasted kWaitFastPolls polls, so a wait that succeeds quickly never loads it.
+__device__ __forceinline__ uint32_t wait_budget(const int32_t* test_ctl) {
+  if (!test_ctl) return kWaitLimit;
+  const int32_t v = *reinterpret_cast<const volatile int32_t*>(test_ctl);
+  return v > 0 ? (uint32_t)v : kWaitLimit;
+}
+
+// Bounded wait: true when the phase completed, false after the poll budget.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const int32_t* test_ctl = nullptr) {
+  for (uint32_t i = 0; i < kWaitFastPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t budget = wait_budget(test_ctl);
+  for (uint32_t i = kWaitFastPolls; i < budget; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+
+// True (once, for one producer) when a test asked this kernel family to withhold one
+// copy: `armed` is the word's [1] as read at kernel start (> 0: a copy is requested).
+__device__ __forceinline__ bool take_withhold(const int32_t* test_ctl, int32_t armed,
+                                              int32_t kinds, int32_t family) {
+  if (!test_ctl || armed <= 0 || !(kinds & family)) return false;
+  return atomicSub(const_cast<int32_t*>(test_ctl) + 1, 1) > 0;
+}
+
+// The word's [1] and [2], read at kernel start (zeros without a word).
+__device__ __forceinline__ void read_withhold(const int32_t* test_ctl, int32_t& armed,
+                                              int32_t& kinds) {
+  armed = 0;
+  kinds = 0;
+  if (test_ctl) {
+    armed = reinterpret_cast<const volatile int32_t*>(test_ctl)[1];
+    kinds = reinterpret_cast<const volatile int32_t*>(test_ctl)[2];
+  }
 }
 
 // Contiguous global -> shared copy of `bytes` (a multiple of 16, both addresses 16-byte

@@ -63,6 +63,8 @@ struct Buffers {
   int32_t* ctl;            // [B] host-uploaded control: bit0 live, bit1 reset position
   int32_t* ctl_pos;        // [B] position applied when bit1 is set
   uint32_t* status;        // [1]
+  int32_t* test_ctl;       // [4] fault-test word (pp_test_faults): poll budget, copies to
+                           // withhold, kernel families; zeros in normal operation
   struct SampleParams* samp;   // [B] sampling parameters (greedy when temperature <= 0)
   int32_t* hist_len;       // [B] text tokens recorded since open (capped at kHist)
   int32_t* hist;           // [B][kHist] text token of position p at p mod kHist
@@ -203,6 +205,7 @@ struct UmmaArgs {
   int ld_op;
   int Bp_out;
   uint32_t* status;
+  const int32_t* test_ctl;   // optional fault-test word (see pp_async.cuh)
   // Fused RMSNorm, producer side (EPI_ADD / EPI_EMB): besides y, write the next
   // contraction's operand hi/lo(norm_alpha * y) [2*Bp][M] and the sums of y^2 over each
   // M-tile's rows, ssq_out[tile * B + b] (the splits of a tile are added in order).
@@ -257,6 +260,7 @@ struct AttnArgs {
   float* part;             // scratch [B*H] blocks of attn_pair_floats(nc_max, Dh)
   uint32_t* count;         // scratch [B*H], zero before the call; left zero after it
   uint32_t* status;        // optional: PP_S_TIMEOUT is raised here when a wait gives up
+  const int32_t* test_ctl; // optional fault-test word (see pp_async.cuh)
   uint16_t* q_op;          // head dim 128: bf16 hi/lo query operand [B*H*2][Dh], already
                            // scaled by q_scale (the tensor-core kernel reads only this)
 };

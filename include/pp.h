@@ -51,7 +51,10 @@ extern "C" {
 /* device-detected conditions (bits of the status word) */
 #define PP_S_NAN 0x1u        /* a logit row held NaN (the NaN entries were not chosen) */
 #define PP_S_INDEX 0x2u      /* an input token was out of range (replaced by the initial token) */
-#define PP_S_TIMEOUT 0x4u    /* a bounded device-side wait gave up */
+#define PP_S_TIMEOUT 0x4u    /* a bounded device-side wait gave up: that tick's columns
+                                and logits are undefined, and so are the ring entries it
+                                wrote, so the sessions open during it should be closed and
+                                reopened; the next tick itself starts clean */
 
 typedef struct {
   int32_t d_model;       /* 4096 */
@@ -136,22 +139,36 @@ int pp_weight_shape(const pp_config* c, int which, int64_t dims[4], int* ndim, i
  * activations, per-step scratch, status word), or 0 for a bad config. */
 size_t pp_workspace_bytes(const pp_config* c);
 
-/* Create an engine.  w: device weight pointers (not copied, must outlive the engine).
+/* Create an engine: the RQ-Transformer of the config (vllm-omni
+ * recipes/NVIDIA/PersonaPlex.md, "Architecture": Helium temporal transformer, depformer
+ * over the 16 codebooks, the [B, 17, 1] column per 80 ms frame) serving up to max_batch
+ * sessions in lockstep (same page, "Notes": elastic batching over a fixed set of slots;
+ * mhpq 运维要点, one ring KV per slot).
+ * w: device weight pointers (not copied, must outlive the engine).
  * workspace: device memory of at least pp_workspace_bytes(c) bytes, 256-byte aligned,
  * owned by the caller.  Captures the whole tick as one CUDA graph.  All slots start
  * closed.  Errors: PP_EINVAL, PP_E_NOSPACE, PP_E_CUDA. */
 int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t ws_bytes,
               pp_engine** out);
 
+/* Release the engine's host state, its CUDA graph, streams and events.  The weights and
+ * the workspace stay the caller's (they are not freed).  Work still queued on the
+ * caller's streams must have finished.  NULL is ignored.  No counterpart on the pages
+ * beyond the engine's lifetime. */
 void pp_destroy(pp_engine* e);
 
-/* Open slot `slot` for a new session at position 0 (the slot's ring contents are
- * ignored from then on because attention reads only positions written since open;
- * a recycled slot behaves exactly like a fresh engine).  Takes effect at the next
- * pp_step.  Errors: PP_E_RANGE (slot >= max_batch), PP_E_BUSY (already open). */
+/* Open slot `slot` for a new session at position 0: admission of a session into the
+ * lockstep batch (vllm-omni PersonaPlex recipe, "Notes": sessions join and leave an
+ * elastic batch, and a recycled slot is bit-exact with a fresh engine; mhpq 运维要点,
+ * per-slot recycle).  The slot's ring contents are ignored from then on because
+ * attention reads only positions written since open, so a recycled slot behaves exactly
+ * like a fresh engine.  Takes effect at the next pp_step.
+ * Errors: PP_E_RANGE (slot >= max_batch), PP_E_BUSY (already open). */
 int pp_session_open(pp_engine* e, int slot);
 
-/* Close slot `slot` at the next pp_step.  Errors: PP_E_RANGE, PP_E_NOTLIVE. */
+/* Close slot `slot` at the next pp_step: the session leaves the elastic batch (same
+ * passages as pp_session_open); from then on the slot's column rows are -1 and it
+ * writes no KV.  Errors: PP_E_RANGE, PP_E_NOTLIVE. */
 int pp_session_close(pp_engine* e, int slot);
 
 /* Open slot `slot` resuming a session at absolute position pos (0 <= pos < 2^31-1):
@@ -248,11 +265,34 @@ int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_c
                  float* logits, void* stream);
 
 /* Wait for `stream`, then read and clear the device status word into *bits
- * (PP_S_* flags).  Errors: PP_E_CUDA. */
+ * (PP_S_* flags).  The pages define no error reporting; the conditions are this
+ * library's (an index or NaN the greedy decision of the recipe's "Notes" would meet, a
+ * bounded wait).  Deliberately an out-parameter rather than a return value, so that the
+ * return value stays the host-side error code of every other call.
+ * Errors: PP_E_CUDA. */
 int pp_status(pp_engine* e, void* stream, uint32_t* bits);
 
 /* Number of kernel launches one pp_step makes (the nodes of the captured graph). */
 int pp_step_kernel_count(pp_engine* e);
+
+/* ---- failure-detection tests --------------------------------------------------------
+ * Lets a test make the tick's bounded device-side waits run out without faulting the
+ * GPU: it lowers the poll budget of every bounded wait and asks producers of the named
+ * kernel families to withhold copies, so that a consumer's wait on a copy that never
+ * comes gives up, the kernel raises PP_S_TIMEOUT, drains its copies, frees its tensor
+ * memory and returns.  This call has no counterpart on the pages.
+ *   wait_polls  poll budget of each bounded wait; 0 restores the default (2^24 polls,
+ *               seconds); a wait reads it only after 1024 unsuccessful polls
+ *   withhold    copies still to withhold: the first producer of a named family to start
+ *               takes one (its first activation tile in a contraction, its first V tile
+ *               in the attention), and so on until none are left; 0 withholds nothing
+ *   kinds       PP_TEST_UMMA and/or PP_TEST_ATTN
+ * Stream-ordered on `stream`; the engine's graph is unchanged.  Reset with (0, 0, 0)
+ * after the test.  Errors: PP_EINVAL, PP_E_CUDA. */
+#define PP_TEST_UMMA 0x1   /* the tensor-core weight contractions */
+#define PP_TEST_ATTN 0x2   /* the ring attention (both kernels) */
+int pp_test_faults(pp_engine* e, int32_t wait_polls, int32_t withhold, int32_t kinds,
+                   void* stream);
 
 /* Kernel families of one tick, for pp_profile_step. */
 enum pp_kernel_kind {
@@ -305,6 +345,9 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
  *              cannot describe returns PP_EINVAL
  *   n_valid    int32 [B], device; values above W count as W, values <= 0 give zeros
  *   out        f32 [B][H*D], device
+ *   status     optional device word (may be NULL): PP_S_TIMEOUT is OR-ed into it when a
+ *              bounded wait inside the kernel gave up (the output is then incomplete);
+ *              with NULL such a timeout goes unreported
  *   scratch    device memory of at least pp_ring_attention_scratch_bytes(B, H, D, W)
  *              bytes, 256-byte aligned, caller-owned; its contents need no set-up
  * D (head_dim) is 32, 64 or 128.  Asynchronous on `stream`.  Errors: PP_EINVAL,
@@ -312,7 +355,8 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
 size_t pp_ring_attention_scratch_bytes(int B, int H, int head_dim, int window);
 int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int64_t slot_stride,
                       const int32_t* n_valid, int B, int H, int head_dim, int window,
-                      float* out, void* scratch, size_t scratch_bytes, void* stream);
+                      float* out, uint32_t* status, void* scratch, size_t scratch_bytes,
+                      void* stream);
 
 /* pp_ring_attention for callers that cannot allocate device memory or pass scratch:
  * for example a host whose device memory all belongs to a pooling allocator that a
@@ -320,8 +364,8 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
  * (it can synchronise the device and take milliseconds) would break the 80 ms cadence.
  * The pages have no counterpart to this call; it exists for those callers.
  * Same arguments and result as pp_ring_attention, minus the scratch: the partials and
- * tickets live in one device array built into the library (about 25.4 MiB, held on
- * every GPU that loads the library until the process exits).  Limits: B*H <= 2048,
+ * tickets live in one device array built into the library (27,795,456 bytes, about
+ * 26.5 MiB, held on every GPU that loads the library until the process exits).  Limits: B*H <= 2048,
  * window <= 3072, head_dim <= 128; larger sizes return PP_E_RANGE.  The first call on
  * a device looks up the array's device address (make that first call before any
  * stream capture).  Every call shares the array, so calls that overlap on the GPU
@@ -329,7 +373,8 @@ int pp_ring_attention(const float* q, const uint16_t* k, const uint16_t* v, int6
  * Allocates no memory.  Errors: PP_EINVAL, PP_E_RANGE, PP_E_CUDA. */
 int pp_ring_attention_noalloc(const float* q, const uint16_t* k, const uint16_t* v,
                               int64_t slot_stride, const int32_t* n_valid, int B, int H,
-                              int head_dim, int window, float* out, void* stream);
+                              int head_dim, int window, float* out, uint32_t* status,
+                              void* stream);
 
 /* ---- session driver: host bookkeeping around pp_step ------------------------------
  * Admission and recycle of slots, the persona / voice prefill and the acoustic delay,

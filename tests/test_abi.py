@@ -129,3 +129,10 @@ def test_binding_structs_match_the_header_layout(tmp_path):
         assert got[(name, "size")] == ctypes.sizeof(cls), name
         for f in cls._fields_:
             assert got[(name, f[0])] == getattr(cls, f[0]).offset, (name, f[0])
+
+
+def test_fault_test_word_rejects_bad_arguments():
+    """pp_test_faults validates on the host (a null engine, negative counts, unknown
+    kernel families) before it touches the device."""
+    lib = pp.lib()
+    assert lib.pp_test_faults(None, 0, 0, 0, None) == pp.PP_EINVAL

@@ -27,11 +27,13 @@ def _run(B, H, D, W, n_valid, seed):
     nbytes = pp.pp_ring_attention_scratch_bytes(B, H, D, W)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(2):   # the second call must find its scratch reusable as left
         pp.pp_ring_attention(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), H * W * D,
-                             dn.data_ptr(), B, H, D, W, out.data_ptr(), scratch.data_ptr(),
-                             nbytes, stream)
+                             dn.data_ptr(), B, H, D, W, out.data_ptr(), status.data_ptr(),
+                             scratch.data_ptr(), nbytes, stream)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0   # no bounded wait gave up
     return q, k, v, out.cpu().numpy().reshape(B, H, D)
 
 
@@ -97,4 +99,4 @@ def test_ring_attention_rejects_bad_arguments():
     with pytest.raises(pp.PPError):
         pp.pp_ring_attention_scratch_bytes(4, 2, 48, 100)
     with pytest.raises(pp.PPError):
-        pp.pp_ring_attention(0, 0, 0, 0, 0, 1, 1, 64, 10, 0, 0, 0, None)
+        pp.pp_ring_attention(0, 0, 0, 0, 0, 1, 1, 64, 10, 0, 0, 0, 0, None)

@@ -103,7 +103,9 @@ def test_sample_rows_match_oracle(case):
             assert got[r] in alts, (r, got[r], alts)
         else:
             assert got[r] == want, (r, got[r], want, kept)
-    assert amb_rows <= (2 * rows) // 3       # most rows are compared exactly
+    # which rows are ambiguous depends on the oracle alone: 0 to 16 of the 64 rows (25 %)
+    # in these cases, so at most a third may be, and the rest are compared exactly
+    assert amb_rows <= rows // 3
     assert bool(st & 1) == (kind == "nonfinite")   # PP_S_NAN only where NaN was present
 
 

@@ -103,3 +103,52 @@ def test_nan_logits_are_flagged_and_never_chosen():
     ocol, olt, _ = orc.step(orc.new_session(), prev[0], user[0])
     assert col[0, 0] == ocol[0] == oracle.argmax_f32(olt)
     assert col[0, 0] != 123
+
+
+@pytest.mark.parametrize("shape_name,family", [("tiny", "attn"), ("small", "attn"),
+                                               ("tiny", "umma"), ("small", "umma")])
+def test_bounded_wait_runs_out_and_the_engine_recovers(shape_name, family):
+    """A producer withholds one copy under a short poll budget (pp_test_faults): the
+    consumer's bounded wait gives up, the tick still returns, and PP_S_TIMEOUT is reported.
+    With the test word reset, sessions reopened in the same slots then give, tick for
+    tick, bitwise the columns and logits of the same sessions in a fresh engine.  The
+    tiny model's attention runs on the CUDA cores (head dim 64), the small model's on the
+    tensor cores (head dim 128)."""
+    import time
+
+    import full_duplex_speech_lockstep_gb300 as pp
+    s = synth.PRESETS[shape_name]
+    kinds = pp.PP_TEST_ATTN if family == "attn" else pp.PP_TEST_UMMA
+    wd = device_weights(synth.make_weights_host(s, 33))
+    eng = pp.Engine(s, 2, wd)
+    ref = pp.Engine(s, 2, wd)
+    T = 5
+    user = synth.uniform_i32((T + 2) * 2 * 8, 33, 9, 0, s.audio_card).reshape(T + 2, 2, 8)
+    init = np.tile(initial_column(s), (2, 1))
+    eng.open(0)
+    eng.open(1)
+    col, _ = _step(eng, s, init, user[0])
+    eng.test_faults(wait_polls=4096, withhold=1, kinds=kinds)
+    t0 = time.time()
+    _step(eng, s, col, user[1])          # returns: the wait ran out, nothing hangs
+    took = time.time() - t0
+    st = eng.status()
+    assert st & pp.PP_S_TIMEOUT, st
+    assert st & ~(pp.PP_S_TIMEOUT | pp.PP_S_NAN) == 0, st
+    assert took < 30.0, took
+    eng.test_faults(0, 0, 0)
+    for e in (eng, ref):
+        if e is eng:
+            e.close(0)
+            e.close(1)
+        e.open(0)
+        e.open(1)
+    pe, pr = init, init
+    for t in range(T):
+        ce, le = _step(eng, s, pe, user[t + 2])
+        cr, lr = _step(ref, s, pr, user[t + 2])
+        assert np.array_equal(ce, cr), t
+        assert np.array_equal(le, lr), t
+        pe, pr = ce, cr
+    assert eng.status() == 0
+    assert ref.status() == 0
