@@ -65,6 +65,8 @@ PP_FLAG_CUDA_CORE_GEMM = 0x1
 PP_FLAG_NO_PDL = 0x2
 PP_FLAG_TWO_GROUPS = 0x4
 PP_FLAG_SKIP_USER_STEPS = 0x8
+PP_FLAG_SEQUENTIAL_USER_STEPS = 0x10
+PP_FLAG_WIDE_TILES = 0x20
 
 
 class pp_sampling(ctypes.Structure):

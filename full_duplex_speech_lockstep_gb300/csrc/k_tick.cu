@@ -293,7 +293,12 @@ __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step
   pdl_wait_and_trigger();
   const int s = blockIdx.x, row = step + 1;
   if (!b.live[s]) {
-    if (threadIdx.x == 0) { b.out_col[s * kRows + row] = -1; b.tok[s] = 0; }
+    if (threadIdx.x == 0) {
+      b.out_col[s * kRows + row] = -1;
+      b.tok[s] = 0;
+      if (D.dep_batched && step == D.dep_steps - 1)
+        for (int c = 0; c < kDepBatch; ++c) b.tokb[(size_t)c * D.B + s] = 0;
+    }
     return;
   }
   int t = 0;
@@ -318,6 +323,16 @@ __global__ void __launch_bounds__(1024) k_dep_argmax(Dims D, Buffers b, int step
     if (t < 0 || t > D.Va) { atomicOr(b.status, PP_S_INDEX); t = D.Va; }
     b.out_col[s * kRows + row] = t;
     b.tok[s] = t;
+    if (D.dep_batched && step == D.dep_steps - 1) {
+      // the tokens of the batched steps: row 8 (just decided), then the user codes of
+      // rows 9..15
+      b.tokb[s] = t;
+      for (int c = 1; c < kDepBatch; ++c) {
+        int u = b.in_user[s * PP_USER_ROWS + c - 1];
+        if (u < 0 || u > D.Va) u = D.Va;   // flagged where the user rows are written
+        b.tokb[(size_t)c * D.B + s] = u;
+      }
+    }
   }
 }
 
@@ -451,6 +466,91 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+// ---- the batched user steps -------------------------------------------------------------
+// Steps 8..15 of a frame take known tokens (row 8, then the user codes), so they run as one
+// pass: for each slot and head this stores the k, v of every batched step at its step
+// index of the frame's cache, then step 8 + c attends over steps 0..8+c with the same
+// arithmetic, in the same order, as the one-step kernel above.
+template <int E>  // head dim / 32
+__global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
+  pdl_wait_and_trigger();
+  const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (h >= D.Hd) return;
+  const int k0 = D.nq - kDepBatch;
+  const size_t op_chunk = (size_t)2 * D.Bp * D.dd;
+  if (!b.live[s]) {
+    for (int c = 0; c < kDepBatch; ++c)
+      for (int e = 0; e < E; ++e) {
+        const int i = h * D.Dhd + lane + 32 * e;
+        b.dout_b[((size_t)c * D.B + s) * D.dd + i] = 0.f;
+        op_store(b.op_dob + c * op_chunk, D.dd, D.Bp, s, i, 0.f);
+      }
+    return;
+  }
+  float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
+  for (int c = 0; c < kDepBatch; ++c) {
+    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      cache[(size_t)(k0 + c) * 2 * D.dd + h * D.Dhd + lane + 32 * e] = row[D.dd + lane + 32 * e];
+      cache[(size_t)(k0 + c) * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] =
+          row[2 * D.dd + lane + 32 * e];
+    }
+  }
+  __syncwarp();
+  const float scale = 1.0f / sqrtf((float)D.Dhd);
+  for (int c = 0; c < kDepBatch; ++c) {
+    const int step = k0 + c;
+    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
+    float q[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) q[e] = row[lane + 32 * e];
+    float sc[16];
+    float m = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      if (t > step) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        dot = fmaf(q[e], cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e], dot);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      sc[t] = dot * scale;
+      m = fmaxf(m, sc[t]);
+    }
+    float l = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      if (t > step) break;
+      const float p = expf(sc[t] - m);
+      l += p;
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        acc[e] = fmaf(p, cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e], acc[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float v = acc[e] / l;
+      const int i = h * D.Dhd + lane + 32 * e;
+      b.dout_b[((size_t)c * D.B + s) * D.dd + i] = v;
+      op_store(b.op_dob + c * op_chunk, D.dd, D.Bp, s, i, v);
+    }
+  }
+}
+
+cudaError_t launch_dep_attn_batch(const Dims& D, const Buffers& b, int layer, cudaStream_t s) {
+  const int threads = D.Hd * 32;
+  switch (D.Dhd) {
+    case 32: return launch_k(k_dep_attn_b<1>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
+    case 64: return launch_k(k_dep_attn_b<2>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
+    case 128: return launch_k(k_dep_attn_b<4>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Rows 9..16 straight from this frame's user codes (when depformer steps 8..15, whose

@@ -12,8 +12,9 @@
 //
 // One CTA = one (M-tile, K-split) unit, 4 warps, two CTAs per SM; the splits of a tile
 // are one cluster:
-//   warp 0 lane 0  TMA producer: weight tile (two 64-row boxes) + activation tile per
-//                  64-wide k-block into a ring of shared-memory stages (128B swizzle);
+//   warp 0 lane 0  TMA producer: weight tile (one 128-row box; gate/up pairs: two
+//                  64-row boxes) + activation tile per 64-wide k-block into a ring of
+//                  shared-memory stages (128B swizzle);
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per k-block into a TMEM
 //                  accumulator [128 lanes x N columns], tcgen05.commit frees the stage;
 //   all 4 warps    epilogue: tcgen05.ld of their 32 TMEM lanes, hi + lo, then either
@@ -61,25 +62,51 @@ __device__ __forceinline__ void epi_store(const UmmaArgs& a, int b, int m, float
   }
 }
 
-template <int N>
+// N: MMA columns (2 x padded slots, hi and lo); H: 128-row halves of the weight tile.
+// H = 1: 4 warps, two CTAs per SM; H = 2: 8 warps, one CTA per SM, a 256-row tile whose
+// two halves share every activation tile (half the activation bytes per weight byte).
+template <int N, int H>
 struct Cfg {
-  static constexpr int kABytes = 128 * kBK * 2;          // 16 KB weight tile
+  static constexpr int kRows = 128 * H;                  // weight rows per tile
+  static constexpr int kPairs = 64 * H;                  // gate/up pairs per tile
+  static constexpr int kThreads = 128 * H;
+  static constexpr int kABytes = kRows * kBK * 2;        // weight tile (H x 16 KB)
   static constexpr int kBBytes = N * kBK * 2;            // activation tile
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (96 * 1024) / kStageBytes < 8 ? (96 * 1024) / kStageBytes : 8;
-  static constexpr int kTmemCols = N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256));
+  static constexpr int kBudget = (H == 1 ? 96 : 192) * 1024;
+  static constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;
+  static constexpr int kCols = H * N;                    // accumulator columns (TMEM)
+  static constexpr int kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, 1/rms*/;
-  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][132] floats, then
-  // the pushed slice sums [kMaxSplits][64] floats at 72 KB
-  static_assert(2 * (N / 2) * 132 * 4 <= 72 * 1024, "epilogue partials overlap the push area");
-  static_assert(72 * 1024 + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
+  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][kPR] floats, then
+  // the pushed slice sums [kMaxSplits][64] floats at kPushOff
+  static constexpr int kPR = kRows + 4;                  // row stride of a parked partial
+  static constexpr int kPushOff = ((2 * (N / 2) * kPR * 4) + 1023) / 1024 * 1024;
+  static_assert(kPushOff + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
+  // single split: SiLU exchange [kPairs][N/2] and y^2 [kRows][N/2 + 1] in the stages
+  static_assert(kRows * (N / 2 + 1) * 4 <= kStages * kStageBytes, "y^2 area");
+  static_assert(kStages >= 2, "pipeline depth");
 };
 
-template <int N>
-__global__ void __launch_bounds__(128, 2)
-    k_umma(const UmmaArgs a, const __grid_constant__ CUtensorMap mapA,
+template <int N, int H>
+__global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
+    k_umma(const UmmaArgs a_in, const __grid_constant__ CUtensorMap mapA,
            const __grid_constant__ CUtensorMap mapB) {
-  using C = Cfg<N>;
+  using C = Cfg<N, H>;
+  // column chunk c: this chunk's operand rows, weights and outputs
+  const int chunk = blockIdx.y;
+  UmmaArgs a = a_in;
+  if (chunk) {
+    a.row0 += chunk * a.a_chunk_rows;
+    if (a.Y) a.Y += chunk * a.y_chunk;
+    if (a.norm_op) a.norm_op += chunk * a.op_chunk;
+    if (a.op_out) a.op_out += chunk * a.op_chunk;
+    if (a.ssq_out) a.ssq_out += chunk * a.ssq_out_chunk;
+    if (a.ssq_in) a.ssq_in += chunk * a.ssq_in_chunk;
+    if (a.emb) a.emb += chunk * a.emb_chunk;
+    if (a.tok) a.tok += chunk * a.tok_chunk;
+  }
+  const int brow = chunk * a.b_chunk_rows;   // first operand row of this chunk
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -117,14 +144,15 @@ __global__ void __launch_bounds__(128, 2)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  // rows of the two 64-row weight boxes of this tile
+  // rows of the weight boxes of this tile: the tile's kRows rows (boxes of 128 rows),
+  // or its kPairs gate rows then the matching up rows (boxes of kPairs rows)
   int rowA0, rowA1;
-  if (a.pair_rows) {            // gate rows then the matching up rows
-    rowA0 = a.row0 + mt * 64;
-    rowA1 = a.row0 + a.pair_rows + mt * 64;
+  if (a.pair_rows) {
+    rowA0 = a.row0 + mt * C::kPairs;
+    rowA1 = a.row0 + a.pair_rows + mt * C::kPairs;
   } else {
-    rowA0 = a.row0 + mt * 128;
-    rowA1 = rowA0 + 64;
+    rowA0 = a.row0 + mt * C::kRows;
+    rowA1 = rowA0 + 128;
   }
 
   if (warp == 0 && lane == 0) {
@@ -135,13 +163,17 @@ __global__ void __launch_bounds__(128, 2)
     int32_t armed, kinds;
     read_withhold(a.test_ctl, armed, kinds);   // used after the dependency wait
     const int pre = nkb < C::kStages ? nkb : C::kStages;
+    // weight tile of one k-block, [kRows][64] swizzled: H boxes of 128 rows, or (gate/up
+    // pairs) a box of the gate rows and a box of the up rows, kPairs rows each
+    auto load_a = [&](uint8_t* sa, int kx, uint32_t full) {
+      tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
+      if (a.pair_rows || H == 2) tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+    };
     for (int i = 0; i < pre; ++i) {
       uint8_t* sa = smem + i * C::kStageBytes;
       const uint32_t full = smem_u32(&bars[i]);
       mbar_expect_tx(full, C::kStageBytes);
-      const int kx = (kb0 + i) * kBK;
-      tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
-      tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+      load_a(sa, (kb0 + i) * kBK, full);
     }
     pdl_wait_and_trigger();
     int issued = 0;
@@ -159,13 +191,12 @@ __global__ void __launch_bounds__(128, 2)
       const int kx = (kb0 + i) * kBK;
       if (i >= pre) {
         mbar_expect_tx(full, C::kStageBytes);
-        tma_load_2d(smem_u32(sa), &mapA, kx, rowA0, full);
-        tma_load_2d(smem_u32(sa + C::kABytes / 2), &mapA, kx, rowA1, full);
+        load_a(sa, kx, full);
       }
       // a failure-detection test may have this producer withhold the first activation
       // tile: its stage never completes and the MMA issuer's bounded wait runs out
       if (!(i == 0 && take_withhold(a.test_ctl, armed, kinds, PP_TEST_UMMA)))
-        tma_load_2d(smem_u32(sb), &mapB, kx, 0, full);
+        tma_load_2d(smem_u32(sb), &mapB, kx, brow, full);
       ++issued;
     }
     if (*abort_flag) {  // drain this CTA's copies still in flight (bounded waits)
@@ -186,9 +217,11 @@ __global__ void __launch_bounds__(128, 2)
       const uint32_t sa = smem_u32(smem + s * C::kStageBytes);
       const uint32_t sb = sa + C::kABytes;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(tmem, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), idesc,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+      for (int h = 0; h < H; ++h)
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(tmem + h * N, smem_desc(sa + h * 16384 + kk * 32), smem_desc(sb + kk * 32),
+                    idesc, (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit(smem_u32(&bars[C::kStages + s]));
     }
     umma_commit(smem_u32(&bars[2 * C::kStages]));
@@ -196,7 +229,7 @@ __global__ void __launch_bounds__(128, 2)
     pdl_wait_and_trigger();
     // fused RMSNorm of the input: 1/rms of every slot, summed from the producer's
     // partials in slice order while the main loop runs
-    for (int b = threadIdx.x - 64; b < a.B; b += 64) {
+    for (int b = threadIdx.x - 64; b < a.B; b += C::kThreads - 64) {
       float rs;
       if (a.rstd_in) {
         rs = a.rstd_in[b];
@@ -227,18 +260,23 @@ __global__ void __launch_bounds__(128, 2)
   const bool ok = !*abort_flag && nkb > 0;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-  const int r = warp * 32 + lane;            // TMEM lane = tile row
+  // this thread: TMEM lane r of accumulator half `half`, i.e. row tr of the tile
+  const int half = warp >> 2;
+  const int r = (warp & 3) * 32 + lane;
+  const int tr = half * 128 + r;
   const int B = a.B, Bp = N / 2;
-  // output row of this thread
+  // output row of this thread: tile row, or pair p (gate when `gate`, else up)
+  const bool gate = (H == 1) ? (r < 64) : (half == 0);
+  const int p = (H == 1) ? (r & 63) : r;
   int m;
-  if (a.pair_rows) m = mt * 64 + (r & 63);   // gate (r < 64) or up (r >= 64) of row m
-  else m = mt * 128 + r;
+  if (a.pair_rows) m = mt * C::kPairs + p;
+  else m = mt * C::kRows + tr;
   const bool row_ok = a.pair_rows ? (m < a.pair_rows) : (m < a.M);
 
   float acc[N / 2];
   {
     uint32_t hi[N / 2], lo[N / 2];
-    const uint32_t t = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t t = tmem + ((uint32_t)((warp & 3) * 32) << 16) + half * N;
     if (ok) {
 #pragma unroll
       for (int c = 0; c < N / 2; c += 8) {
@@ -258,29 +296,31 @@ __global__ void __launch_bounds__(128, 2)
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols));
-  if (!ok && a.splits == 1 && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
 
   // ---- final epilogue, single split: straight from the accumulator registers ------------
   if (a.splits == 1) {
-    if (!ok) return;
+    if (!ok) {
+      if (threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
+      return;
+    }
     if (norm_in) {
 #pragma unroll
       for (int b = 0; b < N / 2; ++b)
         if (b < B) acc[b] *= s_rstd[b];
     }
     if (a.epi == EPI_SILU) {
-      float* xch = reinterpret_cast<float*>(smem);     // stages are idle now: [64][Bp] up values
-      if (r >= 64) {
+      float* xch = reinterpret_cast<float*>(smem);   // stages idle now: [kPairs][Bp] up values
+      if (!gate) {
 #pragma unroll
         for (int b = 0; b < N / 2; ++b)
-          if (b < B) xch[(r - 64) * Bp + b] = acc[b];
+          if (b < B) xch[p * Bp + b] = acc[b];
       }
       __syncthreads();
-      if (r < 64 && row_ok) {
+      if (gate && row_ok) {
 #pragma unroll
         for (int b = 0; b < N / 2; ++b) {
           if (b < B) {
-            const float g = acc[b], u = xch[r * Bp + b];
+            const float g = acc[b], u = xch[p * Bp + b];
             op_store(a.op_out, a.ld_op, a.Bp_out, b, m, g / (1.0f + expf(-g)) * u);
           }
         }
@@ -296,7 +336,7 @@ __global__ void __launch_bounds__(128, 2)
     }
     // producer of a fused RMSNorm: y, the next operand and the tile's sums of y^2
     constexpr int PB1 = N / 2 + 1;
-    float* sq = reinterpret_cast<float*>(smem);      // [128][PB1] y^2, stages idle now
+    float* sq = reinterpret_cast<float*>(smem);      // [kRows][PB1] y^2, stages idle now
 #pragma unroll
     for (int b = 0; b < N / 2; ++b) {
       if (b < B) {
@@ -306,13 +346,13 @@ __global__ void __launch_bounds__(128, 2)
           a.Y[(size_t)b * a.ldy + m] = y;
           op_store(a.norm_op, a.M, Bp, b, m, a.norm_alpha[m] * y);
         }
-        sq[r * PB1 + b] = y * y;
+        sq[tr * PB1 + b] = y * y;
       }
     }
     __syncthreads();
     if (threadIdx.x < B) {
       float ss = 0.f;
-      for (int rr = 0; rr < 128; ++rr) ss += sq[rr * PB1 + threadIdx.x];
+      for (int rr = 0; rr < C::kRows; ++rr) ss += sq[rr * PB1 + threadIdx.x];
       a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
     }
     return;
@@ -324,24 +364,25 @@ __global__ void __launch_bounds__(128, 2)
   // to 4 per thread and step, reading the S partials through distributed shared memory
   // with 16-byte loads and adding them in split order 0..S-1; then it applies the
   // epilogue.  Every CTA passes both cluster barriers, also after a timeout.
-  constexpr int PR = 132;                    // row stride of a parked partial (16 bytes)
+  constexpr int PR = C::kPR;                 // row stride of a parked partial (16 bytes)
   float* mine = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int b = 0; b < N / 2; ++b)
-    if (b < B) mine[b * PR + r] = ok ? acc[b] : 0.f;
+    if (b < B) mine[b * PR + tr] = ok ? acc[b] : 0.f;
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int S = a.splits;
   // y^2 sums of each split's slice, pushed into rank 0's idle stage memory (fused RMSNorm)
-  float* s_push = reinterpret_cast<float*>(smem + 72 * 1024);   // [kMaxSplits][B]
+  float* s_push = reinterpret_cast<float*>(smem + C::kPushOff);   // [kMaxSplits][B]
   const float* peer[kMaxSplits];
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? cluster.map_shared_rank(mine, q) : mine;
   auto ld4 = [](const float* p) { return *reinterpret_cast<const float4*>(p); };
   constexpr int CH = 2;   // 4-row units per thread and step: up to 2*S 16-byte peer loads
   if (a.epi == EPI_SILU) {
-    // slice of the 64 gate/up pairs in whole 4-pair groups; unit = (slot, 4 pairs)
-    const int p0 = 4 * ((sp * 16) / S), p1 = 4 * (((sp + 1) * 16) / S);
+    // slice of the kPairs gate/up pairs in whole 4-pair groups; unit = (slot, 4 pairs);
+    // gate of pair p parked at row p, its up at row kPairs + p
+    const int p0 = 4 * ((sp * (C::kPairs / 4)) / S), p1 = 4 * (((sp + 1) * (C::kPairs / 4)) / S);
     const int G = (p1 - p0) / 4;
     const int n = G * B;
     for (int u0 = threadIdx.x; u0 < n; u0 += CH * (int)blockDim.x) {
@@ -351,7 +392,7 @@ __global__ void __launch_bounds__(128, 2)
         const int u = u0 + i * (int)blockDim.x;
         const int g = u % G;
         bc[i] = u / G;
-        mm[i] = (u < n) ? mt * 64 + p0 + 4 * g : a.pair_rows;   // pair_rows: no unit
+        mm[i] = (u < n) ? mt * C::kPairs + p0 + 4 * g : a.pair_rows;   // pair_rows: no unit
         off[i] = bc[i] * PR + p0 + 4 * g;
       }
       float4 gv[CH][kMaxSplits], uv[CH][kMaxSplits];
@@ -361,7 +402,7 @@ __global__ void __launch_bounds__(128, 2)
         for (int q = 0; q < kMaxSplits; ++q)
           if (q < S && mm[i] < a.pair_rows) {
             gv[i][q] = ld4(peer[q] + off[i]);
-            uv[i][q] = ld4(peer[q] + off[i] + 64);
+            uv[i][q] = ld4(peer[q] + off[i] + C::kPairs);
           }
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
@@ -384,9 +425,9 @@ __global__ void __launch_bounds__(128, 2)
       }
     }
   } else {
-    // slice of the tile's 128 rows in whole 4-row groups; unit = (slot, 4 rows); units
+    // slice of the tile's kRows rows in whole 4-row groups; unit = (slot, 4 rows); units
     // run rows fastest across threads, so y and the next operand are written in rows
-    const int r0 = 4 * ((sp * 32) / S), r1 = 4 * (((sp + 1) * 32) / S);
+    const int r0 = 4 * ((sp * (C::kRows / 4)) / S), r1 = 4 * (((sp + 1) * (C::kRows / 4)) / S);
     const int G = (r1 - r0) / 4;
     const int n = G * B;
     float* sq = mine + (N / 2) * PR;  // [slot][row - r0] y^2 of this slice (fused RMSNorm)
@@ -397,7 +438,7 @@ __global__ void __launch_bounds__(128, 2)
         const int u = u0 + i * (int)blockDim.x;
         const int g = u % G;
         bcol[i] = u / G;
-        mrow[i] = (u < n) ? mt * 128 + r0 + 4 * g : a.M;   // a.M marks "no unit"
+        mrow[i] = (u < n) ? mt * C::kRows + r0 + 4 * g : a.M;   // a.M marks "no unit"
         off[i] = bcol[i] * PR + r0 + 4 * g;
       }
       float4 ex[CH], al[CH];   // residual (or embedding) and norm gains of the 4 rows
@@ -491,20 +532,24 @@ __global__ void __launch_bounds__(128, 2)
 
 }  // namespace
 
-template <int N>
+template <int N, int H>
 static cudaError_t umma_n(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                           cudaStream_t s) {
   const int grid = a.m_tiles * a.splits;
-  return launch_k(k_umma<N>, dim3(grid), dim3(128), Cfg<N>::kSmem, s, a.splits, a, mA, mB);
+  return launch_k(k_umma<N, H>, dim3(grid, a.chunks > 1 ? a.chunks : 1), dim3(Cfg<N, H>::kThreads),
+                  Cfg<N, H>::kSmem, s, a.splits, a, mA, mB);
 }
 
 template <int N>
 static cudaError_t setup_n() {
-  return cudaFuncSetAttribute(k_umma<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<N>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_umma<N, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<N, 1>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_umma<N, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<N, 2>::kSmem);
 }
 
-// Raise the dynamic shared-memory limit of the kernel for N (call before capture).
+// Raise the dynamic shared-memory limits of the kernels for N (call before capture).
 cudaError_t umma_setup(int N) {
   switch (N) {
     case 16: return setup_n<16>();
@@ -519,32 +564,25 @@ cudaError_t umma_setup(int N) {
   }
 }
 
-cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
-                        cudaStream_t s) {
-  switch (a.N) {
-    case 16: return umma_n<16>(a, mA, mB, s);
-    case 32: return umma_n<32>(a, mA, mB, s);
-    case 48: return umma_n<48>(a, mA, mB, s);
-    case 64: return umma_n<64>(a, mA, mB, s);
-    case 80: return umma_n<80>(a, mA, mB, s);
-    case 96: return umma_n<96>(a, mA, mB, s);
-    case 112: return umma_n<112>(a, mA, mB, s);
-    case 128: return umma_n<128>(a, mA, mB, s);
-    default: return cudaErrorInvalidValue;
-  }
+template <int N>
+static cudaError_t umma_h(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
+                          cudaStream_t s) {
+  return a.halves == 2 ? umma_n<N, 2>(a, mA, mB, s) : umma_n<N, 1>(a, mA, mB, s);
 }
 
-int umma_stage_count(int n) {
-  switch (n) {
-    case 16: return Cfg<16>::kStages;
-    case 32: return Cfg<32>::kStages;
-    case 48: return Cfg<48>::kStages;
-    case 64: return Cfg<64>::kStages;
-    case 80: return Cfg<80>::kStages;
-    case 96: return Cfg<96>::kStages;
-    case 112: return Cfg<112>::kStages;
-    case 128: return Cfg<128>::kStages;
-    default: return 0;
+cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
+                        cudaStream_t s) {
+  if (a.halves != 1 && a.halves != 2) return cudaErrorInvalidValue;
+  switch (a.N) {
+    case 16: return umma_h<16>(a, mA, mB, s);
+    case 32: return umma_h<32>(a, mA, mB, s);
+    case 48: return umma_h<48>(a, mA, mB, s);
+    case 64: return umma_h<64>(a, mA, mB, s);
+    case 80: return umma_h<80>(a, mA, mB, s);
+    case 96: return umma_h<96>(a, mA, mB, s);
+    case 112: return umma_h<112>(a, mA, mB, s);
+    case 128: return umma_h<128>(a, mA, mB, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

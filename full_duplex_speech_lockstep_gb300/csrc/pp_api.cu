@@ -39,13 +39,17 @@ struct Prof {
 
 // One family of tensor-core contractions (one stacked weight tensor).
 struct Mm {
-  CUtensorMap mapA;    // stacked weights [rows_total, K] bf16, box 64 k x 64 rows
+  CUtensorMap mapA;    // stacked weights [rows_total, K] bf16, box 64 k x 128 rows
+                       // (gate/up pairs: 64 rows)
   CUtensorMap mapB;    // activation operand [2*Bp, K] bf16, box 64 k x 2*Bp rows
   int M = 0, K = 0, kblocks = 0, splits = 1, m_tiles = 0, pair = 0;
+  int H = 1;           // 128-row halves per weight tile
 };
 
 enum MmKind { MM_QKV, MM_O, MM_GU, MM_DOWN, MM_TEXT, MM_DIN, MM_DQKV, MM_DO, MM_DGU, MM_DDOWN,
-              MM_DHEAD, MM_COUNT };
+              MM_DHEAD,
+              // the depformer's batched user steps: one chunk of operand rows per step
+              MM_BDIN, MM_BDQKV, MM_BDO, MM_BDGU, MM_BDDOWN, MM_BDHEAD, MM_COUNT };
 
 constexpr int kMaxGroups = 2;
 
@@ -56,6 +60,7 @@ constexpr int kMaxGroups = 2;
 // way whatever the group size, so grouping does not change any session's bits.
 struct Group {
   int slot0 = 0;
+  bool wide_tiles = false;  // 256-row weight tiles for the large temporal matrices
   Dims D;
   Buffers buf;
   Mm mm[MM_COUNT];
@@ -120,7 +125,11 @@ Dims make_dims(const pp_config* c) {
   D.eps = c->eps; D.rope_base = c->rope_base;
   D.nc_max = (c->window + kAttnChunk - 1) / kAttnChunk;
   D.logits_ld = c->text_vocab + c->n_q * c->audio_card;
-  D.dep_steps = (c->flags & PP_FLAG_SKIP_USER_STEPS) ? c->n_q / 2 : c->n_q;
+  // the user steps run as one batched pass on the tensor-core path unless elided or
+  // asked to run one at a time
+  const bool tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
+  D.dep_batched = tensor && !(c->flags & (PP_FLAG_SKIP_USER_STEPS | PP_FLAG_SEQUENTIAL_USER_STEPS));
+  D.dep_steps = ((c->flags & PP_FLAG_SKIP_USER_STEPS) || D.dep_batched) ? c->n_q / 2 : c->n_q;
   D.samp_text = (int64_t)c->text_vocab * 4 <= kSampleSmemMax;
   D.samp_audio = (int64_t)c->audio_card * 4 <= kSampleSmemMax;
   return D;
@@ -213,6 +222,10 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.dkv = cv.take<float>(Bs * D.Ld * D.nq * 2 * D.dd);
     b.dout = cv.take<float>(Bs * D.dd);
     b.dh = cv.take<float>(Bs * D.Fd);
+    b.tokb = cv.take<int32_t>(kDepBatch * Bs);
+    b.y_b = cv.take<float>(kDepBatch * Bs * D.dd);
+    b.dqkv_b = cv.take<float>(kDepBatch * Bs * 3 * D.dd);
+    b.dout_b = cv.take<float>(kDepBatch * Bs * D.dd);
     const size_t R = 2 * (size_t)D.Bp;
     b.op_d = cv.take<uint16_t>(R * D.d);
     b.op_o = cv.take<uint16_t>(R * D.d);
@@ -221,6 +234,9 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.op_dd = cv.take<uint16_t>(R * D.dd);
     b.op_do = cv.take<uint16_t>(R * D.dd);
     b.op_fd = cv.take<uint16_t>(R * D.Fd);
+    b.op_ddb = cv.take<uint16_t>(kDepBatch * R * D.dd);
+    b.op_dob = cv.take<uint16_t>(kDepBatch * R * D.dd);
+    b.op_fdb = cv.take<uint16_t>(kDepBatch * R * D.Fd);
     b.ssq = cv.take<float>((size_t)kMaxUnits * Bs);
     b.rstd_z = cv.take<float>(Bs);
     if (grp) {
@@ -309,8 +325,8 @@ namespace {
 // in waves of two CTAs per SM; a unit costs its k-blocks plus a fixed overhead of about
 // five k-blocks (launch share, pipeline fill, epilogue; calibrated on GB300 by sweeping
 // the split counts of the full-size matrices at 64 slots).
-int choose_splits(int m_tiles, int kblocks, int nsm) {
-  const int slots = 2 * nsm;
+int choose_splits(int m_tiles, int kblocks, int nsm, int per_sm) {
+  const int slots = per_sm * nsm;
   int best = 1;
   double best_t = 1e300;
   for (int sp = 1; sp <= kblocks && sp <= kMaxSplits && m_tiles * sp <= kMaxUnits; ++sp) {
@@ -322,19 +338,26 @@ int choose_splits(int m_tiles, int kblocks, int nsm) {
   return best;
 }
 
+// chunks: column chunks of one launch (the split count accounts for all of them);
+// op_chunks: operand chunks the B map spans (1 when the chunks share one operand);
+// H: 128-row halves per weight tile (a function of the matrix shape only, so that every
+// engine size reduces in the same order)
 bool plan_mm(Mm* g, const void* w, int rows_total, int M, int K, int pair, const uint16_t* op,
-             int Bp, int nsm) {
+             int Bp, int nsm, int chunks = 1, int op_chunks = 1, int H = 1) {
   g->M = M;
   g->K = K;
   g->pair = pair;
+  g->H = H;
   // the split-K epilogue moves rows in aligned groups of 4
   if (!pair && M % 4) return false;
   g->kblocks = (K + 63) / 64;
-  g->m_tiles = pair ? (pair + 63) / 64 : (M + 127) / 128;
+  g->m_tiles = pair ? (pair + 64 * H - 1) / (64 * H) : (M + 128 * H - 1) / (128 * H);
   if (g->m_tiles > kMaxTiles) return false;
-  g->splits = choose_splits(g->m_tiles, g->kblocks, nsm);
-  return make_map(&g->mapA, w, (uint64_t)rows_total, (uint64_t)K, 64) &&
-         make_map(&g->mapB, op, (uint64_t)2 * Bp, (uint64_t)K, 2 * Bp);
+  g->splits = choose_splits(g->m_tiles * chunks, g->kblocks, nsm, H == 1 ? 2 : 1);
+  // weight boxes: 128 rows (one 16 KB copy each), or 64 rows for the gate/up pairs of a
+  // 128-row tile
+  return make_map(&g->mapA, w, (uint64_t)rows_total, (uint64_t)K, (pair && H == 1) ? 64 : 128) &&
+         make_map(&g->mapB, op, (uint64_t)op_chunks * 2 * Bp, (uint64_t)K, 2 * Bp);
 }
 
 bool plan_all(Group* e, int nsm) {
@@ -342,17 +365,33 @@ bool plan_all(Group* e, int nsm) {
   const Buffers& b = e->buf;
   const int Bp = D.Bp;
   bool ok = true;
-  ok &= plan_mm(&e->mm[MM_QKV], b.wqkv, D.L * 3 * D.d, 3 * D.d, D.d, 0, b.op_d, Bp, nsm);
-  ok &= plan_mm(&e->mm[MM_O], b.wo, D.L * D.d, D.d, D.d, 0, b.op_o, Bp, nsm);
-  ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, nsm);
-  ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, nsm);
-  ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, nsm);
+  // with wide tiles, the temporal layers' matrices and the text head take 256-row tiles
+  // whose halves share each activation tile
+  const int Ht = e->wide_tiles ? 2 : 1;
+  ok &= plan_mm(&e->mm[MM_QKV], b.wqkv, D.L * 3 * D.d, 3 * D.d, D.d, 0, b.op_d, Bp, nsm, 1, 1, Ht);
+  ok &= plan_mm(&e->mm[MM_O], b.wo, D.L * D.d, D.d, D.d, 0, b.op_o, Bp, nsm, 1, 1, Ht);
+  ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, nsm, 1, 1, Ht);
+  ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, nsm, 1, 1, Ht);
+  ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, nsm, 1, 1, Ht);
   ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_dd, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_do, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_dd, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DDOWN], b.dep_wdown, D.Ld * D.dd, D.dd, D.Fd, 0, b.op_fd, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_dd, Bp, nsm);
+  if (D.dep_batched) {
+    const int nb = kDepBatch;
+    ok &= plan_mm(&e->mm[MM_BDIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, nsm, nb, 1);
+    ok &= plan_mm(&e->mm[MM_BDQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_ddb, Bp,
+                  nsm, nb, nb);
+    ok &= plan_mm(&e->mm[MM_BDO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_dob, Bp, nsm, nb, nb);
+    ok &= plan_mm(&e->mm[MM_BDGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_ddb, Bp, nsm,
+                  nb, nb);
+    ok &= plan_mm(&e->mm[MM_BDDOWN], b.dep_wdown, D.Ld * D.dd, D.dd, D.Fd, 0, b.op_fdb, Bp, nsm,
+                  nb, nb);
+    ok &= plan_mm(&e->mm[MM_BDHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_ddb, Bp, nsm,
+                  nb, nb);
+  }
   return ok;
 }
 
@@ -370,10 +409,29 @@ struct NormIO {
   float* ssq_out = nullptr;
 };
 
+// Column chunks of one launch (the batched depformer steps): strides per chunk.
+struct Chunks {
+  int n = 1;
+  int a_rows = 0, b_rows = 0;
+  long long y = 0, op = 0, emb = 0;
+  int ssq_out = 0, ssq_in = 0, tok = 0;
+  const int32_t* tok_ptr = nullptr;   // tokens of chunk 0 (default: b.tok)
+};
+
 cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, int epi, float* Y,
                       int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s,
-                      const NormIO& nio = NormIO()) {
+                      const NormIO& nio = NormIO(), const Chunks& ch = Chunks()) {
   UmmaArgs a{};
+  a.halves = g.H;
+  a.chunks = ch.n;
+  a.a_chunk_rows = ch.a_rows;
+  a.b_chunk_rows = ch.b_rows;
+  a.y_chunk = ch.y;
+  a.op_chunk = ch.op;
+  a.ssq_out_chunk = ch.ssq_out;
+  a.ssq_in_chunk = ch.ssq_in;
+  a.emb_chunk = ch.emb;
+  a.tok_chunk = ch.tok;
   a.ssq_in = nio.ssq_in;
   a.ssq_nparts = nio.nparts;
   a.ssq_K = nio.K;
@@ -395,7 +453,7 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   a.Y = Y;
   a.ldy = ldy;
   a.emb = emb;
-  a.tok = b.tok;
+  a.tok = ch.tok_ptr ? ch.tok_ptr : b.tok;
   a.op_out = op_out;
   a.ld_op = ld_op;
   a.Bp_out = D.Bp;
@@ -408,6 +466,113 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   do {                                          \
     if (prof) PP_TRY(prof->mark((k), s));       \
   } while (0)
+
+// Depformer steps 8..15 as one batched pass.  Once step 7 has decided row 8, every input
+// of these steps is known (row 8, then the user codes of rows 9..15), and the layers'
+// weights are shared by all steps: each contraction runs once over 8 column chunks, one
+// per step (step 8 + c in chunk c), and the step attention takes all 8 at once.  Each
+// chunk computes exactly what its step computes one at a time: its own in-projection
+// and head, the shared layers, causal attention over steps 0..8+c of the frame.
+cudaError_t enqueue_user_steps_batched(const Group* e, cudaStream_t s, Prof* prof) {
+  const Dims& D = e->D;
+  const Buffers& b = e->buf;
+  const Mm* mm = e->mm;
+  const int nb = kDepBatch, k0 = D.nq - kDepBatch;
+  const int p_din = mm[MM_BDIN].m_tiles;
+  const int p_do = mm[MM_BDO].m_tiles;
+  const int p_ddown = mm[MM_BDDOWN].m_tiles;
+  const long long opd = 2LL * D.Bp * D.dd, opf = 2LL * D.Bp * D.Fd;
+  const int R = 2 * D.Bp;
+  {
+    NormIO in;
+    in.rstd_in = b.rstd_z;
+    in.alpha_out = b.dep_attn_alpha;
+    in.op_next = b.op_ddb;
+    in.ssq_out = b.ssq;
+    Chunks ch;
+    ch.n = nb;
+    ch.a_rows = D.dd;                      // in-projection P_{8+c}
+    ch.y = (long long)D.B * D.dd;
+    ch.op = opd;
+    ch.ssq_out = p_din * D.B;
+    ch.emb = (long long)(D.Va + 1) * D.dd; // audio table 8 + c - 1
+    ch.tok = D.B;
+    ch.tok_ptr = b.tokb;
+    MARK(PP_K_DEP_INPROJ);
+    PP_TRY(mm_launch(D, b, mm[MM_BDIN], k0 * D.dd, EPI_EMB, b.y_b, D.dd,
+                     b.dep_emb_audio + (size_t)(k0 - 1) * (D.Va + 1) * D.dd, nullptr, 0, s, in,
+                     ch));
+  }
+  for (int j = 0; j < D.Ld; ++j) {
+    NormIO qn;
+    qn.ssq_in = b.ssq;
+    qn.nparts = (j == 0) ? p_din : p_ddown;
+    qn.K = D.dd;
+    Chunks cq;
+    cq.n = nb;
+    cq.b_rows = R;
+    cq.y = 3LL * D.B * D.dd;
+    cq.ssq_in = qn.nparts * D.B;
+    MARK(PP_K_DEP_QKV);
+    PP_TRY(mm_launch(D, b, mm[MM_BDQKV], j * 3 * D.dd, EPI_STORE, b.dqkv_b, 3 * D.dd, nullptr,
+                     nullptr, 0, s, qn, cq));
+    MARK(PP_K_DEP_ATTN);
+    PP_TRY(launch_dep_attn_batch(D, b, j, s));
+    NormIO on;
+    on.alpha_out = b.dep_mlp_alpha + (size_t)j * D.dd;
+    on.op_next = b.op_ddb;
+    on.ssq_out = b.ssq;
+    Chunks co;
+    co.n = nb;
+    co.b_rows = R;
+    co.y = (long long)D.B * D.dd;
+    co.op = opd;
+    co.ssq_out = p_do * D.B;
+    MARK(PP_K_DEP_OPROJ);
+    PP_TRY(mm_launch(D, b, mm[MM_BDO], j * D.dd, EPI_ADD, b.y_b, D.dd, nullptr, nullptr, 0, s, on,
+                     co));
+    NormIO gn;
+    gn.ssq_in = b.ssq;
+    gn.nparts = p_do;
+    gn.K = D.dd;
+    Chunks cg;
+    cg.n = nb;
+    cg.b_rows = R;
+    cg.op = opf;
+    cg.ssq_in = p_do * D.B;
+    MARK(PP_K_DEP_GATEUP);
+    PP_TRY(mm_launch(D, b, mm[MM_BDGU], j * 2 * D.Fd, EPI_SILU, nullptr, 0, nullptr, b.op_fdb,
+                     D.Fd, s, gn, cg));
+    NormIO dn;
+    const bool last = (j + 1 == D.Ld);
+    dn.alpha_out = last ? b.dep_out_alpha : b.dep_attn_alpha + (size_t)(j + 1) * D.dd;
+    dn.op_next = b.op_ddb;
+    dn.ssq_out = b.ssq;
+    Chunks cd;
+    cd.n = nb;
+    cd.b_rows = R;
+    cd.y = (long long)D.B * D.dd;
+    cd.op = opd;
+    cd.ssq_out = p_ddown * D.B;
+    MARK(PP_K_DEP_DOWN);
+    PP_TRY(mm_launch(D, b, mm[MM_BDDOWN], j * D.dd, EPI_ADD, b.y_b, D.dd, nullptr, nullptr, 0, s,
+                     dn, cd));
+  }
+  NormIO hn;
+  hn.ssq_in = b.ssq;
+  hn.nparts = p_ddown;
+  hn.K = D.dd;
+  Chunks chd;
+  chd.n = nb;
+  chd.a_rows = D.Va;                       // head H_{8+c}
+  chd.b_rows = R;
+  chd.y = D.Va;                            // its logits follow in the same row
+  chd.ssq_in = p_ddown * D.B;
+  MARK(PP_K_DEP_HEAD);
+  return mm_launch(D, b, mm[MM_BDHEAD], k0 * D.Va, EPI_STORE,
+                   b.logits + D.Vt + (size_t)k0 * D.Va, D.logits_ld, nullptr, nullptr, 0, s, hn,
+                   chd);
+}
 
 // The tick with every weight contraction on the tensor cores.  RMSNorms are fused: each
 // residual-producing contraction writes the next contraction's operand (alpha * y, split
@@ -518,6 +683,7 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_dep_argmax(D, b, k, s));
   }
+  if (D.dep_batched) PP_TRY(enqueue_user_steps_batched(e, s, prof));
   if (D.dep_steps < D.nq) {
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_user_rows(D, b, s));
@@ -772,7 +938,7 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
     err = cudaMemset(b.attn_count, 0, sizeof(uint32_t) * (size_t)D.B * D.H);
     if (err == cudaSuccess) {   // operands: their padding rows stay zero
       char* op_lo = reinterpret_cast<char*>(b.op_d);
-      char* op_hi = reinterpret_cast<char*>(b.op_fd + 2 * (size_t)D.Bp * D.Fd);
+      char* op_hi = reinterpret_cast<char*>(b.op_fdb + (size_t)kDepBatch * 2 * D.Bp * D.Fd);
       err = cudaMemset(op_lo, 0, (size_t)(op_hi - op_lo));
     }
   }
@@ -793,6 +959,7 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
     if (err == cudaSuccess)
       err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+      e->grp[g].wide_tiles = (c->flags & PP_FLAG_WIDE_TILES) != 0;
       err = umma_setup(2 * e->grp[g].D.Bp);
       if (err == cudaSuccess && !plan_all(&e->grp[g], nsm)) err = cudaErrorInvalidValue;
     }

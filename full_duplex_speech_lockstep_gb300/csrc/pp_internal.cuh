@@ -27,7 +27,9 @@ struct Dims {
   int nc_max;            // attention chunks per (slot, head) at a full ring
   int logits_ld;         // Vt + nq * Va
   int Bp;                // slots padded to a multiple of 8: operand rows are [hi: Bp][lo: Bp]
-  int dep_steps;         // depformer steps run (n_q, or n_q / 2 when the user rows are elided)
+  int dep_steps;         // depformer steps run one at a time (n_q, or n_q / 2 when the
+                         // user steps are elided or run as one batched pass)
+  int dep_batched;       // 1: steps n_q/2 .. n_q-1 run as one batched pass
   int samp_text;         // 1: the text decision kernel holds a logit row in shared memory
   int samp_audio;        // 1: the same for the agent audio rows
 };
@@ -94,6 +96,11 @@ struct Buffers {
   float* dkv;              // [B][Ld][nq][2][dd]
   float* dout;             // [B][dd]
   float* dh;               // [B][Fd]
+  // the depformer's batched user steps (steps 8..15, chunk c = step 8 + c)
+  int32_t* tokb;           // [8][B] token feeding step 8 + c
+  float* y_b;              // [8][B][dd]
+  float* dqkv_b;           // [8][B][3dd]
+  float* dout_b;           // [8][B][dd]
   // bf16 hi/lo activation operands of the tensor-core contractions, [2*Bp][K]
   uint16_t* op_d;          // K = d   (normalised temporal stream)
   uint16_t* op_o;          // K = d   (attention output)
@@ -102,6 +109,9 @@ struct Buffers {
   uint16_t* op_dd;         // K = dd  (normalised depformer stream)
   uint16_t* op_do;         // K = dd  (depformer attention output)
   uint16_t* op_fd;         // K = Fd  (depformer gated hidden)
+  uint16_t* op_ddb;        // [8][2*Bp][dd] the same three for the batched user steps
+  uint16_t* op_dob;        // [8][2*Bp][dd]
+  uint16_t* op_fdb;        // [8][2*Bp][Fd]
   float* ssq;              // fused-RMSNorm partial sums of squares [kMaxUnits][B]
   float* rstd_z;           // [B] 1/rms of the temporal output (text head and depformer input)
 };
@@ -188,6 +198,7 @@ __device__ __forceinline__ void op_store(uint16_t* op, int ld, int Bp, int b, in
 
 // Tensor-core contraction (k_umma.cu).
 struct UmmaArgs {
+  int halves;          // 128-row halves of the weight tile: 1 or 2 (a function of the shape)
   int M;               // output rows (EPI_SILU: number of gate/up pairs)
   int pair_rows;       // EPI_SILU: F, the up rows start pair_rows after the gate rows; else 0
   int row0;            // first row of this matrix in the stacked weight tensor map
@@ -221,11 +232,23 @@ struct UmmaArgs {
   float eps;
   const float* rstd_in;
   float* rstd_out;
+  // Independent column chunks (gridDim.y): chunk c runs the same contraction on its own
+  // operand rows and writes its own outputs, each pointer advanced by c times its
+  // stride below (0: the chunks share it).  Used for the depformer steps that run as
+  // one batched pass.
+  int chunks;
+  int a_chunk_rows;        // weight rows between chunks (a different matrix per chunk)
+  int b_chunk_rows;        // operand rows between chunks
+  long long y_chunk;       // floats between chunks' Y
+  long long op_chunk;      // elements between chunks' norm_op / op_out
+  int ssq_out_chunk;       // floats between chunks' ssq_out
+  int ssq_in_chunk;        // floats between chunks' ssq_in
+  long long emb_chunk;     // elements between chunks' embedding tables
+  int tok_chunk;           // entries between chunks' tokens
 };
 cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                         cudaStream_t s);
 cudaError_t umma_setup(int N);
-int umma_stage_count(int N);
 
 enum GemvEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_EMB = 3 };
 struct GemvArgs {
@@ -287,6 +310,9 @@ cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
                             cudaStream_t s);
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s);
+// attention of the batched user steps of one depformer layer
+cudaError_t launch_dep_attn_batch(const Dims& D, const Buffers& b, int layer, cudaStream_t s);
+constexpr int kDepBatch = 8;   // user steps run as one batched pass (n_q / 2)
 cudaError_t sample_setup(const Dims& D);   // shared-memory opt-in of the decision kernels
 cudaError_t launch_sample_rows(const float* logits, int64_t ld, int rows, int n, float temperature,
                                int top_k, float top_p, float penalty, const int32_t* hist,

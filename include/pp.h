@@ -97,6 +97,21 @@ typedef struct {
  * codebook blocks of the logits output) are not computed and keep stale values.  Off by
  * default: the default tick runs all 16 steps. */
 #define PP_FLAG_SKIP_USER_STEPS 0x8
+/* Run depformer steps 8..15 one at a time, as steps 0..7 are.  By default (tensor-core
+ * path) they run as one batched pass: once step 7 has decided row 8, the tokens of steps
+ * 8..15 are known (row 8, then the user codes of rows 9..15), so each contraction and the
+ * step attention process the 8 steps together while every step computes exactly what it
+ * computes alone (its own in-projection and head, causal attention over steps 0..k of
+ * the frame).  Columns and logits agree with the one-at-a-time schedule to fp32
+ * rounding (the batched contractions may split K differently). */
+#define PP_FLAG_SEQUENTIAL_USER_STEPS 0x10
+/* Weight tiles of 256 rows for the temporal layers' matrices and the text head: two
+ * 128-row halves share each activation tile, one CTA (one copy producer) per SM.  Off by
+ * default: on GB300 it measured slower (B=64 tick 22.57 ms against 21.24 ms with the
+ * default 128-row tiles, two CTAs per SM), since a producer streams only about 30 GB/s
+ * and two producers per SM stream twice that.  The tile height changes the K-split, so
+ * a session's bits are reproducible within one setting only. */
+#define PP_FLAG_WIDE_TILES 0x20
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */

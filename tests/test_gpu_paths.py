@@ -79,3 +79,63 @@ def test_skip_user_steps_keeps_every_column():
         runs.append((np.array(cols), np.array(logits)))
     assert np.array_equal(runs[0][0], runs[1][0])
     assert np.array_equal(runs[0][1].view(np.uint32), runs[1][1].view(np.uint32))
+
+
+@pytest.mark.parametrize("B", [5, 64])
+def test_batched_user_steps_match_one_at_a_time(B):
+    """Depformer steps 8..15 as one batched pass (the default) against the same steps run
+    one at a time (PP_FLAG_SEQUENTIAL_USER_STEPS): steps 0..7 and the temporal stack run
+    the same kernels, and steps 8..15 feed nothing back (their rows are the user codes and
+    the cache resets every frame), so every column and the text and agent-step logits are
+    bit-identical; the user steps' logits agree to fp32 rounding (the batched
+    contractions may split K differently)."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    from harness import initial_column
+    s = synth.SMALL
+    w = device_weights(synth.make_weights_host(s, 24, alpha="random"))
+    T = 6
+    Vt, Va = s.text_vocab, s.audio_card
+    ld = Vt + 16 * Va
+    user = synth.uniform_i32(T * B * 8, 5, 5, 0, Va).reshape(T, B, 8)
+    runs = []
+    for flags in [0, pp.PP_FLAG_SEQUENTIAL_USER_STEPS]:
+        e = pp.Engine(s, B, w, flags=flags)
+        for b in range(B):
+            if b % 7 != 3:          # a few closed slots in between
+                e.open(b)
+        prev = torch.from_numpy(np.tile(initial_column(s), (B, 1))).cuda()
+        lg = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+        cols, logits = [], []
+        for t in range(T):
+            col = e.step(prev, torch.from_numpy(user[t]).cuda(), logits=lg)
+            torch.cuda.synchronize()
+            cols.append(col.cpu().numpy().copy())
+            logits.append(lg.cpu().numpy().copy())
+            prev = col.clone()
+        assert e.status() == 0
+        runs.append((np.array(cols), np.array(logits), e.kernel_count()))
+        e.close_engine()
+    (ca, la, na), (cb, lb, nb) = runs
+    assert na < nb                        # the batched pass launches fewer kernels
+    assert np.array_equal(ca, cb)
+    live = [b for b in range(B) if b % 7 != 3]
+    head = Vt + 8 * Va
+    assert np.array_equal(la[:, live, :head].view(np.uint32), lb[:, live, :head].view(np.uint32))
+    ua, ub = la[:, live, head:], lb[:, live, head:]
+    assert np.all(np.isfinite(ua))
+    assert np.max(np.abs(ua - ub)) <= 1e-4 * np.std(ub)   # measured: 1.5e-5
+
+
+@pytest.mark.parametrize("shape_name", ["tiny", "small"])
+def test_wide_tiles_parity(shape_name):
+    """256-row weight tiles (PP_FLAG_WIDE_TILES, two accumulator halves sharing each
+    activation tile) pass the oracle gate; the tiny and small models give ragged tiles
+    (FFN 704 and 1408 gate/up pairs over 128-pair tiles)."""
+    import full_duplex_speech_lockstep_gb300 as pp
+    s = synth.PRESETS[shape_name]
+    w = synth.make_weights_host(s, 25, alpha="random")
+    st = run_parity(s, 3, w, device_weights(w),
+                    [Placement(0, 0, greedy_script(s, 24, 3)), Placement(2, 4, greedy_script(s, 16, 4))],
+                    flags=pp.PP_FLAG_WIDE_TILES)
+    assert st["status"] == 0
