@@ -65,6 +65,12 @@ def parse():
     ap.add_argument("--sampling-steps", type=int, default=50,
                     help="ticks of the secondary measurement with every slot sampled "
                          "(0 = skip it)")
+    ap.add_argument("--latency-ticks", type=int, default=500,
+                    help="ticks of the fixed latency sample (after 20 warm-up ticks) that "
+                         "p50/p99 tick latency are taken over (0 = skip)")
+    ap.add_argument("--staggered-ticks", type=int, default=3750,
+                    help="ticks per session of the staggered B=8 workload (slot i opens at "
+                         "tick 400*i; 3750 = 5 minutes of audio, every ring wraps; 0 = skip)")
     ap.add_argument("--layers", type=int, default=0,
                     help="temporal layers (0 = the shape's own); fewer layers give a small "
                          "case with full-size kernels for profiling")
@@ -289,6 +295,52 @@ def time_ticks(eng, B, shape, steps, warmup, seed_stream):
     return evs[0].elapsed_time(evs[-1]), per
 
 
+def staggered_line(pp, shape, w_dev, flags, ticks, B=8, stride=400):
+    """The staggered B=8 workload at full length: slot i opens at tick stride*i and runs
+    `ticks` ticks of greedy decoding on run/silence user codes, then closes; every tick
+    of the whole schedule is timed with CUDA events on its stream.  Returns the
+    session-frames/s over the schedule and the tick latency percentiles."""
+    import torch
+    from synth import schedules
+    sessions = schedules.staggered_sessions(shape, 3, n_slots=B, stride=stride, T=ticks)
+    horizon = stride * (B - 1) + ticks
+    user = np.zeros((horizon, B, 8), np.int32)
+    for slot, start, u, _, _ in sessions:
+        user[start:start + ticks, slot] = u
+    d_user = torch.from_numpy(user).cuda()
+    eng = pp.Engine(shape, B, w_dev, flags=flags)
+    init = torch.tensor([shape.text_vocab] + [shape.audio_card] * shape.n_q, dtype=torch.int32)
+    prev = init.repeat(B, 1).cuda()
+    cols = [torch.empty((B, 17), dtype=torch.int32, device="cuda") for _ in range(2)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(horizon + 1)]
+    live_ticks = 0
+    torch.cuda.synchronize()
+    evs[0].record()
+    for t in range(horizon):
+        for slot, start, _, _, _ in sessions:
+            if start + ticks == t:
+                eng.close(slot)
+            if start == t:
+                eng.open(slot)
+                prev[slot] = init.cuda()   # a fresh session's first column
+        live_ticks += sum(1 for _, start, _, _, _ in sessions if start <= t < start + ticks)
+        prev = eng.step(prev, d_user[t], out=cols[t % 2])
+        evs[t + 1].record()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(horizon)]
+    total = evs[0].elapsed_time(evs[-1])
+    status = eng.status()
+    eng.close_engine()
+    return {"value": live_ticks / (total / 1000.0), "unit": "session-frames/s",
+            "ticks": horizon, "session_ticks": live_ticks, "ms_total": total,
+            "p50_tick_ms": float(np.percentile(per, 50)),
+            "p99_tick_ms": float(np.percentile(per, 99)),
+            "max_tick_ms": float(np.max(per)), "status_bits": status,
+            "note": "B=8, slot i opens at tick %d*i and runs %d ticks (every ring wraps past "
+                    "%d), greedy, run/silence user codes; includes the host's open/close "
+                    "calls between ticks" % (stride, ticks, shape.window)}
+
+
 def rvq_line(pp, B, iters):
     """pp_rvq_dequantize timed with CUDA events: once on a [B][17] tick column (the
     per-tick use: 8 codebooks of 2048 x 512 fp32) and once on a 65536-frame batch.  The
@@ -372,6 +424,15 @@ def main():
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     tick_gbs = tick_bytes / (ms_per_step / 1000.0) / 1e9
+
+    # -- tick latency over a fixed sample: 20 warm-up ticks, then `latency_ticks` ----------
+    latency = None
+    if a.latency_ticks > 0:
+        _, perl = time_ticks(eng, B, shape, a.latency_ticks, 20, 450 + rank)
+        latency = {"ticks": a.latency_ticks, "warmup": 20,
+                   "p50_ms": float(np.percentile(perl, 50)),
+                   "p99_ms": float(np.percentile(perl, 99)),
+                   "max_ms": float(np.max(perl)), "budget_ms": 80.0}
 
     # -- per-kernel profile through the event-instrumented graph --------------------------
     kind_ms = (ctypes.c_double * len(pp.KERNEL_KINDS))()
@@ -473,6 +534,17 @@ def main():
         b1 = {"session_frames_s": a.b1_steps / (ms1 / 1000.0),
               "p50_ms": float(np.percentile(per1, 50)), "p99_ms": float(np.percentile(per1, 99)),
               "positions": [max(3, a.warmup), max(3, a.warmup) + a.b1_steps]}
+        if a.profile_steps > 0:   # per-kind kernel times of the B=1 tick (event-instrumented)
+            km = (ctypes.c_double * len(pp.KERNEL_KINDS))()
+            kn = (ctypes.c_int64 * len(pp.KERNEL_KINDS))()
+            p1 = init.repeat(1, 1).cuda()
+            c1 = [torch.empty((1, 17), dtype=torch.int32, device="cuda") for _ in range(2)]
+            u1 = torch.from_numpy(synth.uniform_i32(a.profile_steps * 8, SEED, 510, 0,
+                                                    shape.audio_card).reshape(-1, 1, 8)).cuda()
+            for t in range(a.profile_steps):
+                p1 = e1.profile_step(p1, u1[t], km, kn, out=c1[t % 2])
+            b1["kernels_profile_ms_per_tick"] = {
+                k: km[i] / a.profile_steps for i, k in enumerate(pp.KERNEL_KINDS) if kn[i]}
         e1.close_engine()
         if a.skip_user_steps_steps > 0:   # the low-B variant beside the literal 16 steps
             e1 = pp.Engine(shape, 1, w_dev, flags=a.engine_flags | pp.PP_FLAG_SKIP_USER_STEPS)
@@ -482,6 +554,12 @@ def main():
                                      "p50_ms": float(np.percentile(per1, 50)),
                                      "p99_ms": float(np.percentile(per1, 99))}
             e1.close_engine()
+
+    # -- the staggered B=8 workload at full length (every ring wraps) ----------------------
+    staggered = None
+    if a.staggered_ticks > 0 and a.shape == "full":
+        staggered = staggered_line(pp, shape, w_dev, a.engine_flags, a.staggered_ticks)
+        torch.cuda.empty_cache()
 
     # -- CPU oracle baseline (rank 0, N=1 only) -------------------------------------------
     cpu = None
@@ -504,12 +582,14 @@ def main():
                        "l2": "inputs larger than L2 (%.0f GB ring + %.1f GB weights per GPU)"
                              % (B * shape.window * kv_bytes_per_position(shape) / 1e9, wbytes / 1e9)},
             "p50_tick_ms": p50, "p99_tick_ms": p99, "realtime_budget_ms": 80.0,
+            "latency": latency,
             "tick_roofline": {"bytes_per_tick": tick_bytes, "achieved_gbs": tick_gbs,
                               "frac_of_8tbs": tick_gbs / HBM_NOMINAL_GBS,
                               "frac_of_measured": tick_gbs / hbm_peak},
             "roofline": roofline,
             "kernels_profile": prof,
             "b1": b1,
+            "staggered_b8": staggered,
             "skip_user_steps": skip,
             "sampling": samp,
             "rvq": rvq,

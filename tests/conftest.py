@@ -21,3 +21,18 @@ def read_constants():
                 k, v = line.split()
                 out[k] = int(v)
     return out
+
+
+_FULL_WEIGHTS = {}
+
+
+@pytest.fixture(scope="session")
+def full_weights():
+    """Seeded weights of the full PersonaPlex shape, (host numpy, device torch), made once
+    per session for the GPU tests that need them."""
+    if "w" not in _FULL_WEIGHTS:
+        import synth
+        seed = 1
+        _FULL_WEIGHTS["w"] = (synth.make_weights_host(synth.FULL, seed),
+                              synth.make_weights_device(synth.FULL, seed))
+    return _FULL_WEIGHTS["w"]

@@ -55,6 +55,17 @@ class Placement:
     check: bool = True       # False: run on the GPU only (a neighbour, not compared)
 
 
+def device_view(ptr, n, dtype="<i2"):
+    """A torch tensor viewing n elements of device memory at ptr (no copy): used to read
+    engine memory such as a ring block back to the host."""
+    import torch
+
+    class _Mem:
+        __cuda_array_interface__ = {"shape": (int(n),), "typestr": dtype,
+                                    "data": (int(ptr), False), "version": 3}
+    return torch.as_tensor(_Mem(), device="cuda")
+
+
 def device_weights(w_host, device="cuda"):
     import torch
     out = {}

@@ -1,6 +1,7 @@
-"""Parity at the full PersonaPlex shape (GPU): the B=1 prefill workload teacher-forced
-against the oracle, and the bench's launch configuration (64 slots, every ring full at
-3000 positions) with sampled slots checked against the oracle."""
+"""Parity at the full PersonaPlex shape (GPU): the B=1 prefill workload (250 ticks)
+teacher-forced against the oracle, and the bench's launch configuration (64 slots, every
+ring full at 3000 positions) with sampled slots checked against the oracle.  The
+full-shape weights come from the session fixture in conftest.py (seed 1)."""
 import os
 
 import numpy as np
@@ -13,15 +14,10 @@ from harness import Placement, Script, greedy_script, run_parity
 pytestmark = pytest.mark.gpu
 FULL = synth.FULL
 SEED = 1
-TICKS = int(os.environ.get("PP_FULL_TICKS", "40"))   # 250 runs the whole prefill workload
+# the whole prefill workload: 12 voice ticks, 6 silence, 120 persona, 6 silence, free
+# ticks up to 250 (fewer through the environment for a quick look)
+TICKS = int(os.environ.get("PP_FULL_TICKS", "250"))
 FLAGS = int(os.environ.get("PP_FULL_FLAGS", "0"))    # engine flags (1: CUDA-core contractions)
-
-
-@pytest.fixture(scope="module")
-def full_weights():
-    w_dev = synth.make_weights_device(FULL, SEED)
-    w_host = synth.make_weights_host(FULL, SEED)
-    return w_host, w_dev
 
 
 def test_device_generator_matches_host(full_weights):
