@@ -34,12 +34,12 @@ SEED = 5
 HBM_NOMINAL_GBS = 8000.0
 
 # DRAM traffic of the attention kernel from one ncu capture (the --set full capture of one
-# launch at B=8 with a full 3000-position ring, two temporal layers): dram__bytes_read +
+# launch at B=32 with a full 3000-position ring, two temporal layers): dram__bytes_read +
 # dram__bytes_write of that launch per (slot, valid position).  Traffic grows in
 # proportion to the slots, so a full launch's traffic is this times slots x positions.
 # Valid only while k_attn_tc.cu is the source that was captured (its hash below).
-ATTN_TRAFFIC = {"bytes_per_slot_position": (394.677248e6 + 5.22368e6) / (8 * 3000),
-                "source_sha256_16": "90300a4a90da77f6"}
+ATTN_TRAFFIC = {"bytes_per_slot_position": (1574.804e6 + 5.547776e6) / (32 * 3000),
+                "source_sha256_16": "d9b5f27b9abb31ed"}
 
 
 def parse():
@@ -544,6 +544,27 @@ def main():
             for t in range(a.profile_steps):
                 p1 = e1.profile_step(p1, u1[t], km, kn, out=c1[t % 2])
             b1["kernels_profile_ms_per_tick"] = {
+                k: km[i] / a.profile_steps for i, k in enumerate(pp.KERNEL_KINDS) if kn[i]}
+        e1.close_engine()
+        # the low-latency variant: all 16 depformer steps in one persistent kernel
+        e1 = pp.Engine(shape, 1, w_dev, flags=a.engine_flags | pp.PP_FLAG_LOW_LATENCY)
+        e1.open(0)
+        ms1, per1 = time_ticks(e1, 1, shape, a.b1_steps, max(3, a.warmup), 700)
+        b1["low_latency"] = {"session_frames_s": a.b1_steps / (ms1 / 1000.0),
+                             "p50_ms": float(np.percentile(per1, 50)),
+                             "p99_ms": float(np.percentile(per1, 99)),
+                             "note": "PP_FLAG_LOW_LATENCY: the 16 depformer steps in one "
+                                     "persistent kernel (CUDA cores, grid barriers)"}
+        if a.profile_steps > 0:
+            km = (ctypes.c_double * len(pp.KERNEL_KINDS))()
+            kn = (ctypes.c_int64 * len(pp.KERNEL_KINDS))()
+            p1 = init.repeat(1, 1).cuda()
+            c1 = [torch.empty((1, 17), dtype=torch.int32, device="cuda") for _ in range(2)]
+            u1 = torch.from_numpy(synth.uniform_i32(a.profile_steps * 8, SEED, 520, 0,
+                                                    shape.audio_card).reshape(-1, 1, 8)).cuda()
+            for t in range(a.profile_steps):
+                p1 = e1.profile_step(p1, u1[t], km, kn, out=c1[t % 2])
+            b1["low_latency"]["kernels_profile_ms_per_tick"] = {
                 k: km[i] / a.profile_steps for i, k in enumerate(pp.KERNEL_KINDS) if kn[i]}
         e1.close_engine()
         if a.skip_user_steps_steps > 0:   # the low-B variant beside the literal 16 steps

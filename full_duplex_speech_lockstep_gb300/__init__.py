@@ -46,7 +46,7 @@ EXPORTS = ["pp_weight_shape", "pp_workspace_bytes", "pp_create", "pp_destroy",
 # enum pp_kernel_kind
 KERNEL_KINDS = ["begin", "norm", "qkv", "rope_ring", "attn", "oproj", "gateup", "down",
                 "text_head", "dep_inproj", "dep_norm", "dep_qkv", "dep_attn", "dep_oproj",
-                "dep_gateup", "dep_down", "dep_head", "finish"]
+                "dep_gateup", "dep_down", "dep_head", "finish", "dep_persist"]
 
 
 class PPError(RuntimeError):
@@ -67,6 +67,7 @@ PP_FLAG_TWO_GROUPS = 0x4
 PP_FLAG_SKIP_USER_STEPS = 0x8
 PP_FLAG_SEQUENTIAL_USER_STEPS = 0x10
 PP_FLAG_WIDE_TILES = 0x20
+PP_FLAG_LOW_LATENCY = 0x40
 
 
 class pp_sampling(ctypes.Structure):
@@ -249,7 +250,7 @@ def pp_step_kernel_count(h):
     return lib().pp_step_kernel_count(h)
 
 
-PP_TEST_UMMA, PP_TEST_ATTN = 0x1, 0x2
+PP_TEST_UMMA, PP_TEST_ATTN, PP_TEST_PERSIST = 0x1, 0x2, 0x4
 
 
 def pp_test_faults(h, wait_polls, withhold, kinds, stream):

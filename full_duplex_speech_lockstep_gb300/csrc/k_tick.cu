@@ -500,6 +500,16 @@ __global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
     }
   }
   __syncwarp();
+  // every step of the frame in registers: this lane's dims of this head's k and v (steps
+  // 8..15 were stored just above by this lane), loaded at once
+  float kc[16][E], vc[16][E];
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      kc[t][e] = cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
+      vc[t][e] = cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
+    }
   const float scale = 1.0f / sqrtf((float)D.Dhd);
   for (int c = 0; c < kDepBatch; ++c) {
     const int step = k0 + c;
@@ -514,8 +524,7 @@ __global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
       if (t > step) break;
       float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e)
-        dot = fmaf(q[e], cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e], dot);
+      for (int e = 0; e < E; ++e) dot = fmaf(q[e], kc[t][e], dot);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
       sc[t] = dot * scale;
@@ -530,8 +539,7 @@ __global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
       const float p = expf(sc[t] - m);
       l += p;
 #pragma unroll
-      for (int e = 0; e < E; ++e)
-        acc[e] = fmaf(p, cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e], acc[e]);
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vc[t][e], acc[e]);
     }
 #pragma unroll
     for (int e = 0; e < E; ++e) {

@@ -112,6 +112,10 @@ bool config_ok(const pp_config* c) {
   // 16-byte rows for the vectorised weight and activation streams
   if (c->d_model % 8 || c->ffn % 8 || c->dep_d % 8 || c->dep_ffn % 8) return false;
   if (!(c->eps > 0.f) || !(c->rope_base > 1.f)) return false;
+  // the persistent depformer serves small engines on the tensor-core path
+  if ((c->flags & PP_FLAG_LOW_LATENCY) &&
+      (c->max_batch > kPMaxB || (c->flags & PP_FLAG_CUDA_CORE_GEMM)))
+    return false;
   return true;
 }
 
@@ -128,8 +132,11 @@ Dims make_dims(const pp_config* c) {
   // the user steps run as one batched pass on the tensor-core path unless elided or
   // asked to run one at a time
   const bool tensor = !(c->flags & PP_FLAG_CUDA_CORE_GEMM);
-  D.dep_batched = tensor && !(c->flags & (PP_FLAG_SKIP_USER_STEPS | PP_FLAG_SEQUENTIAL_USER_STEPS));
+  D.dep_persist = tensor && (c->flags & PP_FLAG_LOW_LATENCY);
+  D.dep_batched = tensor && !D.dep_persist &&
+                  !(c->flags & (PP_FLAG_SKIP_USER_STEPS | PP_FLAG_SEQUENTIAL_USER_STEPS));
   D.dep_steps = ((c->flags & PP_FLAG_SKIP_USER_STEPS) || D.dep_batched) ? c->n_q / 2 : c->n_q;
+  if (D.dep_persist) D.dep_steps = 0;   // every step runs inside the persistent kernel
   D.samp_text = (int64_t)c->text_vocab * 4 <= kSampleSmemMax;
   D.samp_audio = (int64_t)c->audio_card * 4 <= kSampleSmemMax;
   return D;
@@ -239,6 +246,9 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.op_fdb = cv.take<uint16_t>(kDepBatch * R * D.Fd);
     b.ssq = cv.take<float>((size_t)kMaxUnits * Bs);
     b.rstd_z = cv.take<float>(Bs);
+    b.pbar = cv.take<unsigned>(4);
+    b.ppart_val = cv.take<float>((size_t)kPMaxGrid * kPMaxB);
+    b.ppart_idx = cv.take<int>((size_t)kPMaxGrid * kPMaxB);
     if (grp) {
       grp[g].slot0 = slot0;
       grp[g].D = D;
@@ -631,6 +641,19 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   }
   MARK(PP_K_TEXT_HEAD);
   PP_TRY(launch_text_argmax(D, b, s));
+  if (D.dep_persist) {   // all 16 steps in one persistent kernel
+    PP_TRY(cudaMemsetAsync(b.pbar, 0, 4 * sizeof(unsigned), s));   // barrier words
+    PersistArgs pa;
+    pa.D = D;
+    pa.b = b;
+    pa.bar_count = b.pbar;
+    pa.bar_gen = b.pbar + 1;
+    pa.abort = reinterpret_cast<int*>(b.pbar + 2);
+    pa.part_val = b.ppart_val;
+    pa.part_idx = b.ppart_idx;
+    MARK(PP_K_DEP_PERSIST);
+    PP_TRY(launch_dep_persist(pa, s));
+  }
   g_launch_priority = dep_priority;   // the latency-bound depformer goes first
   for (int k = 0; k < D.dep_steps; ++k) {
     const uint16_t* emb =
@@ -684,7 +707,7 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     PP_TRY(launch_dep_argmax(D, b, k, s));
   }
   if (D.dep_batched) PP_TRY(enqueue_user_steps_batched(e, s, prof));
-  if (D.dep_steps < D.nq) {
+  if (D.dep_steps < D.nq && !D.dep_persist) {
     MARK(PP_K_DEP_HEAD);
     PP_TRY(launch_user_rows(D, b, s));
   }
@@ -952,7 +975,10 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
       if (!gr->has_amaps) err = cudaErrorInvalidValue;
     }
   }
-  for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) err = sample_setup(e->grp[g].D);
+  for (int g = 0; g < e->ngroups && err == cudaSuccess; ++g) {
+    err = sample_setup(e->grp[g].D);
+    if (err == cudaSuccess && e->grp[g].D.dep_persist) err = persist_setup(e->grp[g].D);
+  }
   if (err == cudaSuccess && e->tensor) {
     int dev = 0, nsm = 0;
     err = cudaGetDevice(&dev);
@@ -1061,7 +1087,7 @@ int pp_session_sampling(pp_engine* e, int slot, const pp_sampling* p) {
     if (p->penalty_window < 0 || p->penalty_window > kHist) return PP_EINVAL;
     const Dims& D = e->grp[0].D;
     if (p->text_temperature > 0.f && !D.samp_text) return PP_EINVAL;
-    if (p->audio_temperature > 0.f && !D.samp_audio) return PP_EINVAL;
+    if (p->audio_temperature > 0.f && (!D.samp_audio || D.dep_persist)) return PP_EINVAL;
     sp.t_temp = p->text_temperature;
     sp.t_top_k = p->text_top_k;
     sp.t_top_p = p->text_top_p;
@@ -1215,7 +1241,7 @@ int pp_step_kernel_count(pp_engine* e) { return e ? e->n_kernels : PP_EINVAL; }
 int pp_test_faults(pp_engine* e, int32_t wait_polls, int32_t withhold, int32_t kinds,
                    void* stream) {
   if (!e || wait_polls < 0 || withhold < 0) return PP_EINVAL;
-  if (kinds & ~(PP_TEST_UMMA | PP_TEST_ATTN)) return PP_EINVAL;
+  if (kinds & ~(PP_TEST_UMMA | PP_TEST_ATTN | PP_TEST_PERSIST)) return PP_EINVAL;
   e->test_word[0] = wait_polls;
   e->test_word[1] = withhold;
   e->test_word[2] = kinds;

@@ -30,6 +30,7 @@ struct Dims {
   int dep_steps;         // depformer steps run one at a time (n_q, or n_q / 2 when the
                          // user steps are elided or run as one batched pass)
   int dep_batched;       // 1: steps n_q/2 .. n_q-1 run as one batched pass
+  int dep_persist;       // 1: all depformer steps run as one persistent kernel
   int samp_text;         // 1: the text decision kernel holds a logit row in shared memory
   int samp_audio;        // 1: the same for the agent audio rows
 };
@@ -114,6 +115,10 @@ struct Buffers {
   uint16_t* op_fdb;        // [8][2*Bp][Fd]
   float* ssq;              // fused-RMSNorm partial sums of squares [kMaxUnits][B]
   float* rstd_z;           // [B] 1/rms of the temporal output (text head and depformer input)
+  // the persistent depformer: barrier words (count, generation, abort) and argmax partials
+  unsigned* pbar;          // [4]
+  float* ppart_val;        // [kPMaxGrid][kPMaxB]
+  int* ppart_idx;          // [kPMaxGrid][kPMaxB]
 };
 
 constexpr int kMaxUnits = 4096;      // cap on (M-tile x K-split) units of one contraction
@@ -310,6 +315,22 @@ cudaError_t launch_text_argmax(const Dims& D, const Buffers& b, cudaStream_t s);
 cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer, bool op,
                             cudaStream_t s);
 cudaError_t launch_dep_argmax(const Dims& D, const Buffers& b, int step, cudaStream_t s);
+// The depformer as one persistent kernel (k_dep_persist.cu, PP_FLAG_LOW_LATENCY).
+constexpr int kPMaxB = 8;        // slots of an engine that runs it
+constexpr int kPMaxGrid = 256;   // CTAs (one per SM)
+struct PersistArgs {
+  Dims D;
+  Buffers b;
+  unsigned* bar_count;   // grid barrier: arrivals and generation, zeroed before each launch
+  unsigned* bar_gen;
+  int* abort;            // set by a CTA whose barrier wait gave up
+  float* part_val;       // [kPMaxGrid][kPMaxB] per-CTA argmax partials of a head
+  int* part_idx;         // index | 0x80000000 when the CTA saw a NaN
+};
+size_t persist_smem(const Dims& D);
+cudaError_t persist_setup(const Dims& D);
+cudaError_t launch_dep_persist(const PersistArgs& p, cudaStream_t s);
+
 // attention of the batched user steps of one depformer layer
 cudaError_t launch_dep_attn_batch(const Dims& D, const Buffers& b, int layer, cudaStream_t s);
 constexpr int kDepBatch = 8;   // user steps run as one batched pass (n_q / 2)

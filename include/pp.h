@@ -112,6 +112,14 @@ typedef struct {
  * and two producers per SM stream twice that.  The tile height changes the K-split, so
  * a session's bits are reproducible within one setting only. */
 #define PP_FLAG_WIDE_TILES 0x20
+/* Low-latency depformer for small engines (max_batch <= 8, tensor-core path): the 16
+ * codebook steps run as one persistent kernel, one CTA per SM, phases separated by a
+ * bounded grid barrier, contractions on the CUDA cores in fp32.  It replaces ~300
+ * dependent launches per tick.  Its rounding differs from the default path, so a
+ * session's bits are reproducible among engines with this flag.  Audio sampling is not
+ * available with it (pp_session_sampling returns PP_EINVAL for audio_temperature > 0).
+ * pp_create returns PP_EINVAL for max_batch > 8 or with PP_FLAG_CUDA_CORE_GEMM. */
+#define PP_FLAG_LOW_LATENCY 0x40
 
 /* Weight tensors (device pointers).  Shapes use d = d_model, L = n_layers, F = ffn,
  * Vt = text_vocab, Va = audio_card, dd = dep_d, Ld = dep_layers, Fd = dep_ffn. */
@@ -301,11 +309,13 @@ int pp_step_kernel_count(pp_engine* e);
  *   withhold    copies still to withhold: the first producer of a named family to start
  *               takes one (its first activation tile in a contraction, its first V tile
  *               in the attention), and so on until none are left; 0 withholds nothing
- *   kinds       PP_TEST_UMMA and/or PP_TEST_ATTN
+ *   kinds       PP_TEST_UMMA, PP_TEST_ATTN and/or PP_TEST_PERSIST
  * Stream-ordered on `stream`; the engine's graph is unchanged.  Reset with (0, 0, 0)
  * after the test.  Errors: PP_EINVAL, PP_E_CUDA. */
 #define PP_TEST_UMMA 0x1   /* the tensor-core weight contractions */
 #define PP_TEST_ATTN 0x2   /* the ring attention (both kernels) */
+#define PP_TEST_PERSIST 0x4 /* the persistent depformer: a CTA leaves before its first
+                               grid barrier, so the others' barrier waits run out */
 int pp_test_faults(pp_engine* e, int32_t wait_polls, int32_t withhold, int32_t kinds,
                    void* stream);
 
@@ -329,6 +339,7 @@ enum pp_kernel_kind {
   PP_K_DEP_DOWN,    /* depformer: down-projection + residual */
   PP_K_DEP_HEAD,    /* depformer: per-codebook head + greedy / forced / user row */
   PP_K_FINISH,      /* end-of-tick bookkeeping */
+  PP_K_DEP_PERSIST, /* depformer: all 16 steps in one persistent kernel (PP_FLAG_LOW_LATENCY) */
   PP_K_COUNT
 };
 

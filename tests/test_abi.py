@@ -136,3 +136,13 @@ def test_fault_test_word_rejects_bad_arguments():
     kernel families) before it touches the device."""
     lib = pp.lib()
     assert lib.pp_test_faults(None, 0, 0, 0, None) == pp.PP_EINVAL
+
+
+def test_low_latency_config_limits():
+    """The persistent depformer serves engines of at most 8 slots on the tensor-core path."""
+    ok = pp.make_config(synth.TINY, 8, pp.PP_FLAG_LOW_LATENCY)
+    assert pp.pp_workspace_bytes(ok) > 0
+    for cfg in [pp.make_config(synth.TINY, 9, pp.PP_FLAG_LOW_LATENCY),
+                pp.make_config(synth.TINY, 4, pp.PP_FLAG_LOW_LATENCY | pp.PP_FLAG_CUDA_CORE_GEMM)]:
+        with pytest.raises(pp.PPError):
+            pp.pp_workspace_bytes(cfg)
