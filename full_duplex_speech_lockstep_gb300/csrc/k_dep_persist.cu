@@ -52,38 +52,71 @@ struct Shared {
   int abort;
 };
 
-// Grid barrier on (count, gen): the last CTA to arrive resets the count and advances the
-// generation.  Bounded: a CTA that waits longer than the budget raises the timeout and
-// the global abort; a CTA that sees the abort stops too.  Returns false to stop.
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid barrier on (count, gen): thread 0 of each CTA arrives with a release (after the
+// CTA barrier, so it releases every thread's writes); the last to arrive resets the
+// count and advances the generation with a release; the others poll the generation
+// with acquire loads, spinning first and then sleeping.  Bounded: a CTA that waits
+// longer than the budget raises the timeout and the global abort; a CTA that sees the
+// abort stops too.  Returns false to stop.
 __device__ bool grid_sync(const PersistArgs& p, Shared& sh, uint32_t budget, bool leave = false) {
   __syncthreads();
   if (leave) return false;   // a failure-detection test: this CTA never arrives
   if (threadIdx.x == 0) {
-    volatile unsigned* gen = p.bar_gen;
-    const unsigned g = *gen;
-    __threadfence();
-    if (atomicAdd(p.bar_count, 1u) == gridDim.x - 1) {
-      *p.bar_count = 0u;
-      __threadfence();
-      atomicAdd(const_cast<unsigned*>(gen), 1u);
+    const unsigned g = ld_acquire(p.bar_gen);
+    if (atom_add_acq_rel(p.bar_count, 1u) == gridDim.x - 1) {
+      *reinterpret_cast<volatile unsigned*>(p.bar_count) = 0u;
+      red_add_release(p.bar_gen, 1u);
     } else {
       uint32_t i = 0;
-      while (*gen == g) {
+      while (ld_acquire(p.bar_gen) == g) {
+        if (++i < 512) continue;   // spin first: a phase ends within microseconds
         if (*reinterpret_cast<volatile int*>(p.abort)) { sh.abort = 1; break; }
-        if (++i > budget) {
+        if (i > budget) {
           sh.abort = 1;
           atomicExch(p.abort, 1);
           atomicOr(p.b.status, PP_S_TIMEOUT);
           break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
       }
     }
-    __threadfence();
     if (*reinterpret_cast<volatile int*>(p.abort)) sh.abort = 1;
   }
   __syncthreads();
   return !sh.abort;
+}
+
+// L2 prefetch of this warp's rows of the next phase's matrix (rows m = gw, gw + GW, ...;
+// with `pair`, also row pair + m): issued a phase ahead so that the next phase's row
+// loads meet L2 rather than HBM
+__device__ __forceinline__ void prefetch_rows(const uint16_t* W, int M, int K, int pair, int gw,
+                                              int GW) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint32_t bytes = (uint32_t)K * 2;   // a multiple of 16 (K % 8 == 0)
+  for (int m = gw; m < M; m += GW) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (size_t)m * K), "r"(bytes)
+                 : "memory");
+    if (pair)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (size_t)(pair + m) * K),
+                   "r"(bytes)
+                   : "memory");
+  }
 }
 
 // dot products of weight row `row` (K bf16, 16-byte aligned) with the B staged vectors
@@ -192,6 +225,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
   float v[MAXB];
   for (int k = 0; k < nq; ++k) {
     // ---- in-projection: y = P_k z + D_k[tok], z = x * rstd_z * out_alpha ------------
+    prefetch_rows(b.dep_wqkv, 3 * dd, dd, 0, gw, GW);   // layer 0's qkv
     for (int bb = 0; bb < B; ++bb) {
       const float r = b.rstd_z[bb];
       for (int i = threadIdx.x; i < D.d; i += kPThreads)
@@ -217,6 +251,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
     if (!grid_sync(p, sh, budget, k == 0 && s_leave)) return;
     for (int j = 0; j < D.Ld; ++j) {
       // ---- qkv = W_qkv RMSNorm(y) ------------------------------------------------------
+      prefetch_rows(b.dep_wo + (size_t)j * dd * dd, dd, dd, 0, gw, GW);   // for the o-proj
       stage(b.y, dd, dd, B, b.dep_attn_alpha + (size_t)j * dd, D.eps, xs, sh);
       {
         const uint16_t* W = b.dep_wqkv + (size_t)j * 3 * dd * dd;
@@ -229,48 +264,53 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
       }
       if (!grid_sync(p, sh, budget)) return;
       // ---- attention of step k over the frame's steps 0..k (one warp per slot, head) ----
+      // lane t scores key t (a sequential dot over the head's dims), the lanes take the
+      // softmax over a fixed shuffle tree, then each lane adds p_t v_t over t in order
+      // for its own dims; every load of a step is issued before its first use
       for (int task = gw; task < B * D.Hd; task += GW) {
         const int s = task / D.Hd, h = task - s * D.Hd;
         const float* row = b.dqkv + (size_t)s * 3 * dd + h * D.Dhd;
         float* cache = b.dkv + ((size_t)s * D.Ld + j) * nq * 2 * dd;
-        const int E = D.Dhd >> 5;   // dims per lane (1, 2 or 4)
-        float q[4], kk[4], vv[4];
-        for (int e = 0; e < E; ++e) {
-          q[e] = __ldcg(row + lane + 32 * e);
-          kk[e] = __ldcg(row + dd + lane + 32 * e);
-          vv[e] = __ldcg(row + 2 * dd + lane + 32 * e);
-          cache[(size_t)k * 2 * dd + h * D.Dhd + lane + 32 * e] = kk[e];
-          cache[(size_t)k * 2 * dd + dd + h * D.Dhd + lane + 32 * e] = vv[e];
+        for (int i = lane; i < D.Dhd; i += 32) {
+          cache[(size_t)k * 2 * dd + h * D.Dhd + i] = __ldcg(row + dd + i);
+          cache[(size_t)k * 2 * dd + dd + h * D.Dhd + i] = __ldcg(row + 2 * dd + i);
         }
-        const float scale = 1.0f / sqrtf((float)D.Dhd);
-        float sc[16];
-        float mx = -INFINITY;
-        for (int t = 0; t <= k; ++t) {
+        __syncwarp();
+        float sc = -INFINITY;
+        if (lane <= k) {
+          const float4* q4 = reinterpret_cast<const float4*>(row);
+          const float4* k4 = reinterpret_cast<const float4*>(cache + (size_t)lane * 2 * dd + h * D.Dhd);
           float dot = 0.f;
-          for (int e = 0; e < E; ++e) {
-            const float kt = (t == k) ? kk[e]
-                                      : __ldcg(cache + (size_t)t * 2 * dd + h * D.Dhd + lane + 32 * e);
-            dot = fmaf(q[e], kt, dot);
+          for (int i = 0; i < (D.Dhd >> 2); ++i) {
+            const float4 a = __ldcg(q4 + i), c = __ldcg(k4 + i);
+            dot = fmaf(a.x, c.x, dot);
+            dot = fmaf(a.y, c.y, dot);
+            dot = fmaf(a.z, c.z, dot);
+            dot = fmaf(a.w, c.w, dot);
           }
+          sc = dot * (1.0f / sqrtf((float)D.Dhd));
+        }
+        float mx = sc;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          sc[t] = dot * scale;
-          mx = fmaxf(mx, sc[t]);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float pw = lane <= k ? expf(sc - mx) : 0.f;
+        float l = pw;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        for (int i = lane; i < D.Dhd; i += 32) {
+          float vt[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            vt[t] = t <= k ? __ldcg(cache + (size_t)t * 2 * dd + dd + h * D.Dhd + i) : 0.f;
+          float acc = 0.f;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) acc = fmaf(__shfl_sync(0xffffffffu, pw, t), vt[t], acc);
+          b.dout[(size_t)s * dd + h * D.Dhd + i] = acc / l;
         }
-        float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int t = 0; t <= k; ++t) {
-          const float pw = expf(sc[t] - mx);
-          l += pw;
-          for (int e = 0; e < E; ++e) {
-            const float vt = (t == k) ? vv[e]
-                                      : __ldcg(cache + (size_t)t * 2 * dd + dd + h * D.Dhd + lane + 32 * e);
-            acc[e] = fmaf(pw, vt, acc[e]);
-          }
-        }
-        for (int e = 0; e < E; ++e) b.dout[(size_t)s * dd + h * D.Dhd + lane + 32 * e] = acc[e] / l;
       }
       if (!grid_sync(p, sh, budget)) return;
       // ---- y += W_o o ----------------------------------------------------------------------
+      prefetch_rows(b.dep_wgu + (size_t)j * 2 * Fd * dd, Fd, dd, Fd, gw, GW);   // gate/up
       stage(b.dout, dd, dd, B, nullptr, 0.f, xs, sh);
       {
         const uint16_t* W = b.dep_wo + (size_t)j * dd * dd;
@@ -283,6 +323,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
       }
       if (!grid_sync(p, sh, budget)) return;
       // ---- h = silu(W_g n) * (W_u n), n = RMSNorm(y) ---------------------------------------
+      prefetch_rows(b.dep_wdown + (size_t)j * dd * Fd, dd, Fd, 0, gw, GW);   // for the down
       stage(b.y, dd, dd, B, b.dep_mlp_alpha + (size_t)j * dd, D.eps, xs, sh);
       {
         const uint16_t* W = b.dep_wgu + (size_t)j * 2 * Fd * dd;
@@ -298,6 +339,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
       }
       if (!grid_sync(p, sh, budget)) return;
       // ---- y += W_down h ---------------------------------------------------------------------
+      if (j + 1 < D.Ld)   // the next layer's qkv, or this step's head
+        prefetch_rows(b.dep_wqkv + (size_t)(j + 1) * 3 * dd * dd, 3 * dd, dd, 0, gw, GW);
+      else
+        prefetch_rows(b.dep_heads + (size_t)k * Va * dd, Va, dd, 0, gw, GW);
       stage(b.dh, Fd, Fd, B, nullptr, 0.f, xs, sh);
       {
         const uint16_t* W = b.dep_wdown + (size_t)j * dd * Fd;
@@ -311,6 +356,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_dep_persist(const PersistArgs 
       if (!grid_sync(p, sh, budget)) return;
     }
     // ---- head k: logits and this CTA's argmax partial per slot --------------------------
+    if (k + 1 < nq)   // the next step's in-projection
+      prefetch_rows(b.dep_inproj + (size_t)(k + 1) * dd * D.d, dd, D.d, 0, gw, GW);
     stage(b.y, dd, dd, B, b.dep_out_alpha, D.eps, xs, sh);
     {
       const uint16_t* Hk = b.dep_heads + (size_t)k * Va * dd;

@@ -71,9 +71,12 @@ __global__ void __launch_bounds__(256) k_begin(Dims D, Buffers b, const float* a
     pos_s = b.pos[s];
     b.nvalid[s] = live_s ? min(pos_s + 1, D.W) : 0;
   }
-  // this slot's attention tickets start the tick at zero (the merges leave them zero; a
-  // tick whose bounded wait gave up may not have)
+  // this slot's attention tickets, and the fused decisions' tickets, start the tick at
+  // zero (the kernels leave them zero; a tick whose bounded wait gave up may not have)
   for (int h = threadIdx.x; h < D.H; h += blockDim.x) b.attn_count[(size_t)s * D.H + h] = 0u;
+  if (s == 0 && threadIdx.x < 4) b.dticket[threadIdx.x] = 0u;
+  if (s == 0 && threadIdx.x < 2) b.dnan[threadIdx.x] = 0u;
+  if (threadIdx.x < 2) b.dkey[(size_t)threadIdx.x * D.B + s] = 0ull;
   __syncthreads();
   if (threadIdx.x < kRows) {
     const int r = threadIdx.x;

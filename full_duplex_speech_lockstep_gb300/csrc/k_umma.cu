@@ -65,6 +65,107 @@ __device__ __forceinline__ void epi_store(const UmmaArgs& a, int b, int m, float
 // N: MMA columns (2 x padded slots, hi and lo); H: 128-row halves of the weight tile.
 // H = 1: 4 warps, two CTAs per SM; H = 2: 8 warps, one CTA per SM, a 256-row tile whose
 // two halves share every activation tile (half the activation bytes per weight byte).
+// Order-preserving 64-bit key of a finite logit at a row: a larger value wins, then the
+// lower row (the greedy rule); -0 counts as +0.  Any reduction order gives the same max.
+__device__ __forceinline__ unsigned long long greedy_key(float v, int row) {
+  if (v == 0.f) v = 0.f;
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+}
+
+__device__ __forceinline__ void greedy_add(unsigned long long* best, unsigned* flags, float v, int row) {
+  if (isnan(v)) flags[0] = 1u;
+  else atomicMax(best, greedy_key(v, row));
+}
+
+// The fused greedy decision of a head contraction: each CTA folds its per-slot keys
+// (best[b]) into the launch's global key of each slot with an atomic max, and its NaN
+// flag (flags[0]) into a global flag; the last CTA to finish reads the B keys, resets them
+// for the next launch, and takes each slot's decision (forced token, greedy token, or
+// user code), as the decision kernels of the sampling-capable tick do for greedy slots.
+__device__ void decide_tail(const UmmaArgs& a, unsigned long long* best, unsigned* flags, int B) {
+  const DecideArgs& d = a.dec;
+  const int units = gridDim.x;
+  __syncthreads();
+  if (threadIdx.x < B && best[threadIdx.x]) atomicMax(d.key + threadIdx.x, best[threadIdx.x]);
+  if (threadIdx.x == 0 && flags[0]) atomicOr(d.nan, 1u);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    flags[1] = (atomicAdd(d.ticket, 1u) == (unsigned)units - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!flags[1]) return;
+  __threadfence();
+  if (threadIdx.x < B) {
+    best[threadIdx.x] = __ldcg(d.key + threadIdx.x);
+    d.key[threadIdx.x] = 0ull;   // ready for the next launch
+  }
+  if (threadIdx.x == 0) {
+    flags[0] = __ldcg(d.nan);
+    *d.nan = 0u;
+  }
+  __syncthreads();
+  if (threadIdx.x < B) {
+    const int s = threadIdx.x;
+    const unsigned long long k = best[s];
+    const int am = k ? (int)(0xFFFFFFFFu - (uint32_t)k) : 0;   // all NaN: token 0
+    const bool nan = flags[0] != 0u;
+    if (d.kind == 1) {   // text row 0
+      if (!d.live[s]) {
+        d.out_col[s * kRows] = -1;
+        d.tok[s] = 0;
+      } else {
+        int t = am;
+        if (d.fmask[s * kRows]) {
+          t = d.forced[s * kRows];
+          if (t < 0 || t > d.V) { atomicOr(a.status, PP_S_INDEX); t = d.V; }
+        } else if (nan) {
+          atomicOr(a.status, PP_S_NAN);
+        }
+        d.out_col[s * kRows] = t;
+        d.tok[s] = t;
+        const int pos = d.pos[s];
+        d.hist[(size_t)s * d.hist_ld + (pos & (d.hist_ld - 1))] = t;
+        d.hist_len[s] = min(d.hist_len[s] + 1, d.hist_ld);
+      }
+    } else {             // depformer step `step` decides row step + 1
+      const int row = d.step + 1;
+      if (!d.live[s]) {
+        d.out_col[s * kRows + row] = -1;
+        d.tok[s] = 0;
+        if (d.tokb)
+          for (int c = 0; c < kDepBatch; ++c) d.tok_b[(size_t)c * B + s] = 0;
+      } else {
+        int t;
+        if (row <= PP_AGENT_ROWS) {
+          if (d.fmask[s * kRows + row]) {
+            t = d.forced[s * kRows + row];
+          } else {
+            t = am;
+            if (nan) atomicOr(a.status, PP_S_NAN);
+          }
+        } else {
+          t = d.user[s * PP_USER_ROWS + row - 1 - PP_AGENT_ROWS];
+        }
+        if (t < 0 || t > d.V) { atomicOr(a.status, PP_S_INDEX); t = d.V; }
+        d.out_col[s * kRows + row] = t;
+        d.tok[s] = t;
+        if (d.tokb) {
+          d.tok_b[s] = t;
+          for (int c = 1; c < kDepBatch; ++c) {
+            int u = d.user[s * PP_USER_ROWS + c - 1];
+            if (u < 0 || u > d.V) u = d.V;
+            d.tok_b[(size_t)c * B + s] = u;
+          }
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) *d.ticket = 0u;   // ready for the next launch
+}
+
 template <int N, int H>
 struct Cfg {
   static constexpr int kRows = 128 * H;                  // weight rows per tile
@@ -83,6 +184,9 @@ struct Cfg {
   static constexpr int kPR = kRows + 4;                  // row stride of a parked partial
   static constexpr int kPushOff = ((2 * (N / 2) * kPR * 4) + 1023) / 1024 * 1024;
   static_assert(kPushOff + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
+  // fused greedy decision: [64] keys and 2 flags after the push area
+  static constexpr int kKeyOff = kPushOff + kMaxSplits * 64 * 4;
+  static_assert(kKeyOff + 64 * 8 + 16 <= kStages * kStageBytes, "decision keys");
   // single split: SiLU exchange [kPairs][N/2] and y^2 [kRows][N/2 + 1] in the stages
   static_assert(kRows * (N / 2 + 1) * 4 <= kStages * kStageBytes, "y^2 area");
   static_assert(kStages >= 2, "pipeline depth");
@@ -291,6 +395,12 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
       for (int c = 0; c < N / 2; ++c) acc[c] = 0.f;
     }
   }
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + C::kKeyOff);
+  unsigned* s_dflags = reinterpret_cast<unsigned*>(smem + C::kKeyOff + 64 * 8);
+  if (a.dec.kind) {   // the stages are idle: per-slot best keys of the fused decision
+    if (threadIdx.x < 64) s_best[threadIdx.x] = 0ull;
+    if (threadIdx.x == 0) s_dflags[0] = 0u;
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == 0)
@@ -328,10 +438,17 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
       return;
     }
     if (!norm_out) {
-      if (!row_ok) return;
+      if (row_ok) {
 #pragma unroll
-      for (int b = 0; b < N / 2; ++b)
-        if (b < B) epi_store(a, b, m, acc[b]);
+        for (int b = 0; b < N / 2; ++b)
+          if (b < B) epi_store(a, b, m, acc[b]);
+        if (a.dec.kind) {
+#pragma unroll
+          for (int b = 0; b < N / 2; ++b)
+            if (b < B) greedy_add(&s_best[b], s_dflags, acc[b], m);
+        }
+      }
+      if (a.dec.kind) decide_tail(a, s_best, s_dflags, B);
       return;
     }
     // producer of a fused RMSNorm: y, the next operand and the tile's sums of y^2
@@ -485,6 +602,10 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
         }
         *reinterpret_cast<float4*>(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]) =
             make_float4(y[0], y[1], y[2], y[3]);
+        if (a.dec.kind) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) greedy_add(&s_best[bcol[i]], s_dflags, y[c], mrow[i] + c);
+        }
         if (norm_out) {
           uint16_t hi[4], lo[4];
 #pragma unroll
@@ -528,6 +649,7 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
     a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
   }
   if (!ok && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
+  if (a.dec.kind) decide_tail(a, s_best, s_dflags, B);
 }
 
 }  // namespace

@@ -82,7 +82,9 @@ struct pp_engine {
   cudaEvent_t fork = nullptr, join[kMaxGroups] = {nullptr, nullptr};
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
-  cudaGraphExec_t exec = nullptr;
+  cudaGraphExec_t exec = nullptr;      // the tick with the decision kernels (sampling)
+  cudaGraph_t graph_greedy = nullptr;
+  cudaGraphExec_t exec_greedy = nullptr;   // greedy decisions fused into the heads
   int n_kernels = 0;
   cudaGraph_t prof_graph = nullptr;
   cudaGraphExec_t prof_exec = nullptr;
@@ -246,6 +248,9 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.op_fdb = cv.take<uint16_t>(kDepBatch * R * D.Fd);
     b.ssq = cv.take<float>((size_t)kMaxUnits * Bs);
     b.rstd_z = cv.take<float>(Bs);
+    b.dkey = cv.take<unsigned long long>(2 * Bs);
+    b.dnan = cv.take<unsigned>(2);
+    b.dticket = cv.take<unsigned>(4);
     b.pbar = cv.take<unsigned>(4);
     b.ppart_val = cv.take<float>((size_t)kPMaxGrid * kPMaxB);
     b.ppart_idx = cv.take<int>((size_t)kPMaxGrid * kPMaxB);
@@ -334,7 +339,9 @@ namespace {
 // never of the batch, so every engine size reduces in the same order.  Model: units run
 // in waves of two CTAs per SM; a unit costs its k-blocks plus a fixed overhead of about
 // five k-blocks (launch share, pipeline fill, epilogue; calibrated on GB300 by sweeping
-// the split counts of the full-size matrices at 64 slots).
+// the split counts of the full-size matrices at 64 slots) plus half a k-block per split
+// (the cluster reduction grows with the splits; this moved the small depformer
+// contractions from 8 to 4 splits, -0.25 ms per B=64 tick on GB300).
 int choose_splits(int m_tiles, int kblocks, int nsm, int per_sm) {
   const int slots = per_sm * nsm;
   int best = 1;
@@ -342,7 +349,7 @@ int choose_splits(int m_tiles, int kblocks, int nsm, int per_sm) {
   for (int sp = 1; sp <= kblocks && sp <= kMaxSplits && m_tiles * sp <= kMaxUnits; ++sp) {
     const int units = m_tiles * sp;
     const int waves = (units + slots - 1) / slots;
-    const double t = waves * ((double)((kblocks + sp - 1) / sp) + 5.0);
+    const double t = waves * ((double)((kblocks + sp - 1) / sp) + 5.0 + 0.5 * sp);
     if (t < best_t - 1e-9) { best_t = t; best = sp; }
   }
   return best;
@@ -430,8 +437,10 @@ struct Chunks {
 
 cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, int epi, float* Y,
                       int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s,
-                      const NormIO& nio = NormIO(), const Chunks& ch = Chunks()) {
+                      const NormIO& nio = NormIO(), const Chunks& ch = Chunks(),
+                      const DecideArgs* dec = nullptr) {
   UmmaArgs a{};
+  if (dec) a.dec = *dec;
   a.halves = g.H;
   a.chunks = ch.n;
   a.a_chunk_rows = ch.a_rows;
@@ -584,10 +593,40 @@ cudaError_t enqueue_user_steps_batched(const Group* e, cudaStream_t s, Prof* pro
                    chd);
 }
 
+// The fused greedy decision of a head launch (kind 1: text row 0; kind 2: depformer step
+// `step`).
+bool make_decide(const Dims& D, const Buffers& b, const Mm& g, int kind, int step,
+                 DecideArgs* d) {
+  (void)g;
+  *d = DecideArgs{};
+  d->kind = kind;
+  d->step = step;
+  d->V = kind == 1 ? D.Vt : D.Va;
+  d->tokb = kind == 2 && D.dep_batched && step == D.dep_steps - 1;
+  d->key = b.dkey + (kind == 1 ? 0 : D.B);
+  d->nan = b.dnan + (kind == 1 ? 0 : 1);
+  d->ticket = b.dticket + (kind == 1 ? 0 : 1);
+  d->live = b.live;
+  d->fmask = b.in_fmask;
+  d->forced = b.in_forced;
+  d->user = b.in_user;
+  d->pos = b.pos;
+  d->out_col = b.out_col;
+  d->tok = b.tok;
+  d->tok_b = b.tokb;
+  d->hist = b.hist;
+  d->hist_len = b.hist_len;
+  d->hist_ld = kHist;
+  return true;
+}
+
 // The tick with every weight contraction on the tensor cores.  RMSNorms are fused: each
 // residual-producing contraction writes the next contraction's operand (alpha * y, split
 // bf16) and per-slice sums of y^2; the consuming contraction scales by 1/rms.
-cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s, Prof* prof) {
+// greedy: the greedy-only tick, whose text and depformer heads take their decisions in
+// their own epilogues (no decision kernels; no sampled slot may be open)
+cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s, Prof* prof,
+                                bool greedy) {
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
@@ -636,11 +675,16 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     tn.nparts = p_down;
     tn.K = D.d;
     tn.rstd_out = b.rstd_z;     // kept for the 16 depformer input projections
+    DecideArgs dt;
+    const bool fuse = greedy && make_decide(D, b, mm[MM_TEXT], 1, 0, &dt);
     MARK(PP_K_TEXT_HEAD);
-    PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s, tn));
+    PP_TRY(mm_launch(D, b, mm[MM_TEXT], 0, EPI_STORE, b.logits, D.logits_ld, nullptr, nullptr, 0, s, tn,
+                     Chunks(), fuse ? &dt : nullptr));
+    if (!fuse) {
+      MARK(PP_K_TEXT_HEAD);
+      PP_TRY(launch_text_argmax(D, b, s));
+    }
   }
-  MARK(PP_K_TEXT_HEAD);
-  PP_TRY(launch_text_argmax(D, b, s));
   if (D.dep_persist) {   // all 16 steps in one persistent kernel
     PP_TRY(cudaMemsetAsync(b.pbar, 0, 4 * sizeof(unsigned), s));   // barrier words
     PersistArgs pa;
@@ -700,11 +744,15 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     hn.ssq_in = b.ssq;
     hn.nparts = p_ddown;
     hn.K = D.dd;
+    DecideArgs dh;
+    const bool fuse = greedy && make_decide(D, b, mm[MM_DHEAD], 2, k, &dh);
     MARK(PP_K_DEP_HEAD);
     PP_TRY(mm_launch(D, b, mm[MM_DHEAD], k * D.Va, EPI_STORE, b.logits + D.Vt + (size_t)k * D.Va,
-                     D.logits_ld, nullptr, nullptr, 0, s, hn));
-    MARK(PP_K_DEP_HEAD);
-    PP_TRY(launch_dep_argmax(D, b, k, s));
+                     D.logits_ld, nullptr, nullptr, 0, s, hn, Chunks(), fuse ? &dh : nullptr));
+    if (!fuse) {
+      MARK(PP_K_DEP_HEAD);
+      PP_TRY(launch_dep_argmax(D, b, k, s));
+    }
   }
   if (D.dep_batched) PP_TRY(enqueue_user_steps_batched(e, s, prof));
   if (D.dep_steps < D.nq && !D.dep_persist) {
@@ -821,9 +869,9 @@ cudaError_t enqueue_tick_cc(const Dims& D, const Buffers& b, const AttnMaps* ama
   return cudaSuccess;
 }
 
-cudaError_t enqueue_group(const pp_engine* e, int g, cudaStream_t s, Prof* prof) {
+cudaError_t enqueue_group(const pp_engine* e, int g, cudaStream_t s, Prof* prof, bool greedy) {
   g_launch_priority = 0;
-  cudaError_t err = e->tensor ? enqueue_tick_tensor(&e->grp[g], e->dep_priority, s, prof)
+  cudaError_t err = e->tensor ? enqueue_tick_tensor(&e->grp[g], e->dep_priority, s, prof, greedy)
                               : enqueue_tick_cc(e->grp[g].D, e->grp[g].buf,
                                                 e->grp[g].has_amaps ? &e->grp[g].amaps : nullptr,
                                                 s, prof);
@@ -834,15 +882,15 @@ cudaError_t enqueue_group(const pp_engine* e, int g, cudaStream_t s, Prof* prof)
 // The whole tick: one branch per slot group (a fork/join inside the captured graph);
 // the profiling graph runs the groups one after the other so that its events time
 // single kernels.
-cudaError_t enqueue_tick(const pp_engine* e, cudaStream_t s, Prof* prof) {
+cudaError_t enqueue_tick(const pp_engine* e, cudaStream_t s, Prof* prof, bool greedy) {
   if (e->ngroups == 1 || prof) {
-    for (int g = 0; g < e->ngroups; ++g) PP_TRY(enqueue_group(e, g, s, prof));
+    for (int g = 0; g < e->ngroups; ++g) PP_TRY(enqueue_group(e, g, s, prof, greedy));
     return cudaSuccess;
   }
   PP_TRY(cudaEventRecord(e->fork, s));
   for (int g = 0; g < e->ngroups; ++g) {
     PP_TRY(cudaStreamWaitEvent(e->branch[g], e->fork, 0));
-    PP_TRY(enqueue_group(e, g, e->branch[g], nullptr));
+    PP_TRY(enqueue_group(e, g, e->branch[g], nullptr, greedy));
     PP_TRY(cudaEventRecord(e->join[g], e->branch[g]));
     PP_TRY(cudaStreamWaitEvent(s, e->join[g], 0));
   }
@@ -1005,14 +1053,24 @@ int pp_create(const pp_config* c, const pp_weights* w, void* workspace, size_t w
   if (err == cudaSuccess)
     err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
   if (err == cudaSuccess) {
-    cudaError_t le = enqueue_tick(e, e->cap_stream, nullptr);
+    cudaError_t le = enqueue_tick(e, e->cap_stream, nullptr, false);
     err = cudaStreamEndCapture(e->cap_stream, &e->graph);
     if (le != cudaSuccess) err = le;
   }
   if (err == cudaSuccess) err = cudaGraphInstantiate(&e->exec, e->graph, 0);
+  // the greedy-only tick (the decisions fused into the heads), used while no open slot
+  // samples
+  if (err == cudaSuccess)
+    err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
+  if (err == cudaSuccess) {
+    cudaError_t le = enqueue_tick(e, e->cap_stream, nullptr, true);
+    err = cudaStreamEndCapture(e->cap_stream, &e->graph_greedy);
+    if (le != cudaSuccess) err = le;
+  }
+  if (err == cudaSuccess) err = cudaGraphInstantiate(&e->exec_greedy, e->graph_greedy, 0);
   if (err == cudaSuccess) {
     size_t n = 0;
-    err = cudaGraphGetNodes(e->graph, nullptr, &n);
+    err = cudaGraphGetNodes(e->graph_greedy, nullptr, &n);
     e->n_kernels = (int)n;
   }
   if (err == cudaSuccess) err = cudaDeviceSynchronize();
@@ -1031,6 +1089,8 @@ void pp_destroy(pp_engine* e) {
   e->prof.clear();
   if (e->exec) cudaGraphExecDestroy(e->exec);
   if (e->graph) cudaGraphDestroy(e->graph);
+  if (e->exec_greedy) cudaGraphExecDestroy(e->exec_greedy);
+  if (e->graph_greedy) cudaGraphDestroy(e->graph_greedy);
   if (e->cap_stream) cudaStreamDestroy(e->cap_stream);
   for (int g = 0; g < kMaxGroups; ++g) {
     if (e->branch[g]) cudaStreamDestroy(e->branch[g]);
@@ -1123,6 +1183,13 @@ int pp_ring_block(pp_engine* e, int layer, int slot, int kv, void** ptr) {
   return PP_OK;
 }
 
+// True when an open slot samples a row: the tick then needs the decision kernels.
+static bool any_sampling(const pp_engine* e) {
+  for (int i = 0; i < e->B; ++i)
+    if (e->open[i] && (e->samp[i].t_temp > 0.f || e->samp[i].a_temp > 0.f)) return true;
+  return false;
+}
+
 static int step_impl(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
                      const uint8_t* force_mask, const int32_t* forced_tokens, int32_t* column,
                      float* logits, cudaStream_t s, bool wait, cudaGraphExec_t exec) {
@@ -1175,7 +1242,7 @@ int pp_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
             float* logits, void* stream) {
   if (!e) return PP_EINVAL;
   return step_impl(e, prev_column, user_codes, force_mask, forced_tokens, column, logits,
-                   (cudaStream_t)stream, false, e->exec);
+                   (cudaStream_t)stream, false, any_sampling(e) ? e->exec : e->exec_greedy);
 }
 
 int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
@@ -1183,7 +1250,7 @@ int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_c
                  float* logits, void* stream) {
   if (!e) return PP_EINVAL;
   return step_impl(e, prev_column, user_codes, force_mask, forced_tokens, column, logits,
-                   (cudaStream_t)stream, true, e->exec);
+                   (cudaStream_t)stream, true, any_sampling(e) ? e->exec : e->exec_greedy);
 }
 
 int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* user_codes,
@@ -1194,7 +1261,7 @@ int pp_profile_step(pp_engine* e, const int32_t* prev_column, const int32_t* use
     g_use_pdl = e->pdl;
     cudaError_t err = cudaStreamBeginCapture(e->cap_stream, cudaStreamCaptureModeThreadLocal);
     if (err == cudaSuccess) {
-      cudaError_t le = enqueue_tick(e, e->cap_stream, &e->prof);
+      cudaError_t le = enqueue_tick(e, e->cap_stream, &e->prof, !any_sampling(e));
       err = cudaStreamEndCapture(e->cap_stream, &e->prof_graph);
       if (le != cudaSuccess) err = le;
     }

@@ -116,6 +116,9 @@ struct Buffers {
   float* ssq;              // fused-RMSNorm partial sums of squares [kMaxUnits][B]
   float* rstd_z;           // [B] 1/rms of the temporal output (text head and depformer input)
   // the persistent depformer: barrier words (count, generation, abort) and argmax partials
+  unsigned long long* dkey;   // [2][B] fused-decision keys (text head, depformer heads)
+  unsigned* dnan;          // [2]
+  unsigned* dticket;       // [4]
   unsigned* pbar;          // [4]
   float* ppart_val;        // [kPMaxGrid][kPMaxB]
   int* ppart_idx;          // [kPMaxGrid][kPMaxB]
@@ -201,6 +204,30 @@ __device__ __forceinline__ void op_store(uint16_t* op, int ld, int Bp, int b, in
   op[(size_t)(Bp + b) * ld + k] = lo;
 }
 
+// Greedy decision fused into a head contraction (the greedy-only tick): each CTA keeps,
+// per slot, the best (value, lowest index) of the rows it finalises as one 64-bit key,
+// and the last CTA to finish takes every slot's decision.
+struct DecideArgs {
+  int kind;                  // 0: none; 1: text row 0; 2: depformer row step + 1
+  int step;                  // kind 2: the depformer step
+  int V;                     // logits per row (the forced-token range is 0..V)
+  int tokb;                  // kind 2: also write the batched steps' token table
+  unsigned long long* key;   // [B] the launch's best key per slot, zero between launches
+  unsigned* nan;             // [1] a NaN was seen
+  unsigned* ticket;          // zero before the launch; left zero after it
+  const int32_t* live;
+  const uint8_t* fmask;
+  const int32_t* forced;
+  const int32_t* user;
+  const int32_t* pos;
+  int32_t* out_col;
+  int32_t* tok;
+  int32_t* tok_b;            // [8][B]
+  int32_t* hist;             // kind 1: the repetition-penalty ring [B][hist_ld]
+  int32_t* hist_len;
+  int hist_ld;               // a power of two
+};
+
 // Tensor-core contraction (k_umma.cu).
 struct UmmaArgs {
   int halves;          // 128-row halves of the weight tile: 1 or 2 (a function of the shape)
@@ -250,6 +277,7 @@ struct UmmaArgs {
   int ssq_in_chunk;        // floats between chunks' ssq_in
   long long emb_chunk;     // elements between chunks' embedding tables
   int tok_chunk;           // entries between chunks' tokens
+  DecideArgs dec;          // fused greedy decision (EPI_STORE heads; kind 0: none)
 };
 cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensorMap& mB,
                         cudaStream_t s);

@@ -295,7 +295,12 @@ int pp_step_host(pp_engine* e, const int32_t* prev_column, const int32_t* user_c
  * Errors: PP_E_CUDA. */
 int pp_status(pp_engine* e, void* stream, uint32_t* bits);
 
-/* Number of kernel launches one pp_step makes (the nodes of the captured graph). */
+/* Number of kernel launches one greedy pp_step makes (the nodes of the captured greedy
+ * graph).  The engine holds two graphs of the tick: while no open slot samples, pp_step
+ * runs the greedy one, whose text and depformer heads take their decisions in their own
+ * epilogues (the last CTA of each head reduces every CTA's best (value, lowest index)
+ * key); with a sampled slot open it runs the one with the decision kernels.  Both give a
+ * greedy slot the same bits. */
 int pp_step_kernel_count(pp_engine* e);
 
 /* ---- failure-detection tests --------------------------------------------------------

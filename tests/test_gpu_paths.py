@@ -139,3 +139,53 @@ def test_wide_tiles_parity(shape_name):
                     [Placement(0, 0, greedy_script(s, 24, 3)), Placement(2, 4, greedy_script(s, 16, 4))],
                     flags=pp.PP_FLAG_WIDE_TILES)
     assert st["status"] == 0
+
+
+def test_fused_greedy_decisions_match_decision_kernels():
+    """While no open slot samples, the tick takes its greedy decisions inside the text and
+    depformer head contractions (the last CTA of each head reduces the per-CTA best keys);
+    with a sampled slot open it runs the decision kernels.  The same greedy sessions (one
+    with forced rows, one joining late) in an engine of each kind: bit-identical columns
+    and logits, and the fused tick launches fewer kernels."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    from harness import initial_column
+    from synth import schedules
+    s = synth.SMALL
+    w = device_weights(synth.make_weights_host(s, 26, alpha="random"))
+    B, T = 4, 14
+    Vt, Va = s.text_vocab, s.audio_card
+    ld = Vt + 16 * Va
+    user = synth.uniform_i32(T * B * 8, 6, 6, 0, Va).reshape(T, B, 8)
+    _, fm, fo = schedules.prefill_session(s, 27, T=T, voice=3, persona=4)
+    runs = []
+    for sampled_neighbour in (False, True):
+        e = pp.Engine(s, B, w)
+        e.open(0)
+        if sampled_neighbour:   # slot 3 samples: the tick needs the decision kernels
+            e.open(3)
+            e.set_sampling(3, text_temperature=0.8, audio_temperature=0.5, seed=9)
+        prev = np.tile(initial_column(s), (B, 1))
+        lg = torch.empty((B, ld), dtype=torch.float32, device="cuda")
+        cols, logits = [], []
+        for t in range(T):
+            if t == 3:
+                e.open(1)
+                prev[1] = initial_column(s)   # a fresh session's first column
+            FM = np.zeros((B, 17), np.uint8)
+            FO = np.zeros((B, 17), np.int32)
+            FM[0], FO[0] = fm[t], fo[t]
+            d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+            col = e.step(d(prev), d(user[t]), d(FM), d(FO), logits=lg).cpu().numpy()
+            cols.append(col[:2].copy())
+            logits.append(lg.cpu().numpy()[:2].copy())
+            prev = col.copy()
+            prev[2] = initial_column(s)
+        assert e.status() == 0
+        runs.append((np.array(cols), np.array(logits), e.kernel_count()))
+        e.close_engine()
+    (ca, la, na), (cb, lb, nb) = runs
+    assert np.array_equal(ca, cb)
+    assert np.array_equal(la.view(np.uint32), lb.view(np.uint32))
+    assert na == nb   # kernel_count reports the greedy tick's launches
+    print("kernels per greedy tick", na)
