@@ -392,7 +392,8 @@ cudaError_t sample_setup(const Dims& D) {
 // cache and attends causally over steps 0..step (no positional encoding); the cache is
 // indexed by step, so a new frame overwrites it from step 0 (reset each frame).
 template <int E>  // head dim / 32
-__global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
+__global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E))
+k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
   pdl_wait_and_trigger();
   const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
@@ -406,17 +407,15 @@ __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
   }
   const float* row = b.dqkv + (size_t)s * 3 * D.dd + h * D.Dhd;
   float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
-  float q[E], kk[E], vv[E];
+  // every load first (this step's q, k, v and the frame's earlier steps, all independent),
+  // then the cache append: a store between them would order the later loads after it
+  float q[E], kk[E], vv[E], kc[16][E], vc[16][E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     q[e] = row[lane + 32 * e];
     kk[e] = row[D.dd + lane + 32 * e];
     vv[e] = row[2 * D.dd + lane + 32 * e];
-    cache[(size_t)step * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kk[e];
-    cache[(size_t)step * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] = vv[e];
   }
-  // preload this frame's earlier steps (independent loads), then attend in step order
-  float kc[16][E], vc[16][E];
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
     if (t >= step) break;
@@ -425,6 +424,11 @@ __global__ void k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
       kc[t][e] = cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
       vc[t][e] = cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
     }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    cache[(size_t)step * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kk[e];
+    cache[(size_t)step * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] = vv[e];
   }
   const float scale = 1.0f / sqrtf((float)D.Dhd);
   float sc[16];
@@ -477,7 +481,7 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
 // index of the frame's cache, then step 8 + c attends over steps 0..8+c with the same
 // arithmetic, in the same order, as the one-step kernel above.
 template <int E>  // head dim / 32
-__global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
+__global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E)) k_dep_attn_b(Dims D, Buffers b, int layer) {
   pdl_wait_and_trigger();
   const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
@@ -493,33 +497,42 @@ __global__ void k_dep_attn_b(Dims D, Buffers b, int layer) {
     return;
   }
   float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
-  for (int c = 0; c < kDepBatch; ++c) {
-    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
+  // every step of the frame in registers, this lane's dims of this head: steps 0..k0-1
+  // from the cache, steps k0.. and the queries from this pass's qkv rows, all loaded
+  // before the cache append (a store between them would order the later loads after it)
+  float kc[16][E], vc[16][E], qb[kDepBatch][E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      cache[(size_t)(k0 + c) * 2 * D.dd + h * D.Dhd + lane + 32 * e] = row[D.dd + lane + 32 * e];
-      cache[(size_t)(k0 + c) * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] =
-          row[2 * D.dd + lane + 32 * e];
-    }
-  }
-  __syncwarp();
-  // every step of the frame in registers: this lane's dims of this head's k and v (steps
-  // 8..15 were stored just above by this lane), loaded at once
-  float kc[16][E], vc[16][E];
-#pragma unroll
-  for (int t = 0; t < 16; ++t)
+  for (int t = 0; t < 16; ++t) {
+    if (t >= k0) break;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       kc[t][e] = cache[(size_t)t * 2 * D.dd + h * D.Dhd + lane + 32 * e];
       vc[t][e] = cache[(size_t)t * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e];
     }
+  }
+#pragma unroll
+  for (int c = 0; c < kDepBatch; ++c) {
+    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      qb[c][e] = row[lane + 32 * e];
+      kc[16 - kDepBatch + c][e] = row[D.dd + lane + 32 * e];
+      vc[16 - kDepBatch + c][e] = row[2 * D.dd + lane + 32 * e];
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < kDepBatch; ++c)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      cache[(size_t)(k0 + c) * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kc[16 - kDepBatch + c][e];
+      cache[(size_t)(k0 + c) * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] =
+          vc[16 - kDepBatch + c][e];
+    }
   const float scale = 1.0f / sqrtf((float)D.Dhd);
+#pragma unroll
   for (int c = 0; c < kDepBatch; ++c) {
     const int step = k0 + c;
-    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
-    float q[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) q[e] = row[lane + 32 * e];
+    const float* q = qb[c];
     float sc[16];
     float m = -INFINITY;
 #pragma unroll

@@ -21,7 +21,9 @@
 //                  the final epilogue (one split) or, when the K range is split, a
 //                  reduction across the thread-block cluster formed by the tile's
 //                  splits: partials meet in distributed shared memory and each CTA
-//                  adds them in split order for a slice of the tile's rows.  The split
+//                  adds them in split order for a slice of the tile's rows, then
+//                  arrives at the cluster barrier and finishes its slice before it
+//                  waits there (its peers may still be reading its partial).  The split
 //                  count depends only on the matrix shape and the SM count, never on
 //                  the batch, so a session's bits do not depend on the other sessions.
 // Every mbarrier wait is bounded; on expiry the kernel raises PP_S_TIMEOUT, drains
@@ -74,9 +76,22 @@ __device__ __forceinline__ unsigned long long greedy_key(float v, int row) {
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
 }
 
-__device__ __forceinline__ void greedy_add(unsigned long long* best, unsigned* flags, float v, int row) {
-  if (isnan(v)) flags[0] = 1u;
-  else atomicMax(best, greedy_key(v, row));
+// A warp's candidates, one logit per lane (valid: the lane holds one): the warp's
+// best key (the largest order bits, then the lowest row among the lanes that hold them)
+// goes to shared memory in one atomic instead of 32 colliding ones.  Every lane of the
+// warp calls it.
+__device__ __forceinline__ void greedy_add_warp(unsigned long long* best, unsigned* flags,
+                                                float v, bool valid, int row) {
+  uint32_t hi = 0u;   // 0: no candidate (finite values and infinities map above 0)
+  if (valid) {
+    if (isnan(v)) flags[0] = 1u;
+    else hi = (uint32_t)(greedy_key(v, row) >> 32);
+  }
+  const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (mx == 0u) return;
+  const uint32_t mr = __reduce_min_sync(0xFFFFFFFFu, hi == mx ? (uint32_t)row : 0xFFFFFFFFu);
+  if ((threadIdx.x & 31) == 0)
+    atomicMax(best, ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - mr));
 }
 
 // The fused greedy decision of a head contraction: each CTA folds its per-slot keys
@@ -179,13 +194,10 @@ struct Cfg {
   static constexpr int kCols = H * N;                    // accumulator columns (TMEM)
   static constexpr int kTmemCols = kCols <= 32 ? 32 : (kCols <= 64 ? 64 : (kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512)));
   static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers, 1/rms*/;
-  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][kPR] floats, then
-  // the pushed slice sums [kMaxSplits][64] floats at kPushOff
+  // the split-K epilogue reuses the idle stages: partial + y^2 [2][N/2][kPR] floats
   static constexpr int kPR = kRows + 4;                  // row stride of a parked partial
-  static constexpr int kPushOff = ((2 * (N / 2) * kPR * 4) + 1023) / 1024 * 1024;
-  static_assert(kPushOff + kMaxSplits * 64 * 4 <= kStages * kStageBytes, "push area");
-  // fused greedy decision: [64] keys and 2 flags after the push area
-  static constexpr int kKeyOff = kPushOff + kMaxSplits * 64 * 4;
+  // fused greedy decision: [64] keys and 2 flags after the partials
+  static constexpr int kKeyOff = ((2 * (N / 2) * kPR * 4) + 1023) / 1024 * 1024;
   static_assert(kKeyOff + 64 * 8 + 16 <= kStages * kStageBytes, "decision keys");
   // single split: SiLU exchange [kPairs][N/2] and y^2 [kRows][N/2 + 1] in the stages
   static_assert(kRows * (N / 2 + 1) * 4 <= kStages * kStageBytes, "y^2 area");
@@ -442,13 +454,13 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
 #pragma unroll
         for (int b = 0; b < N / 2; ++b)
           if (b < B) epi_store(a, b, m, acc[b]);
-        if (a.dec.kind) {
-#pragma unroll
-          for (int b = 0; b < N / 2; ++b)
-            if (b < B) greedy_add(&s_best[b], s_dflags, acc[b], m);
-        }
       }
-      if (a.dec.kind) decide_tail(a, s_best, s_dflags, B);
+      if (a.dec.kind) {   // every lane of every warp is here (ok is uniform)
+#pragma unroll
+        for (int b = 0; b < N / 2; ++b)
+          if (b < B) greedy_add_warp(&s_best[b], s_dflags, acc[b], row_ok, m);
+        decide_tail(a, s_best, s_dflags, B);
+      }
       return;
     }
     // producer of a fused RMSNorm: y, the next operand and the tile's sums of y^2
@@ -480,7 +492,9 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
   // after a cluster barrier, CTA `sp` reduces a slice of the tile's rows, 4 rows aligned
   // to 4 per thread and step, reading the S partials through distributed shared memory
   // with 16-byte loads and adding them in split order 0..S-1; then it applies the
-  // epilogue.  Every CTA passes both cluster barriers, also after a timeout.
+  // epilogue.  The second cluster barrier is split: a CTA arrives once it has read its
+  // peers and waits (before it exits, which would free its shared memory) only after
+  // its slice's stores.  Every CTA passes both barriers, also after a timeout.
   constexpr int PR = C::kPR;                 // row stride of a parked partial (16 bytes)
   float* mine = reinterpret_cast<float*>(smem);
 #pragma unroll
@@ -489,8 +503,6 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int S = a.splits;
-  // y^2 sums of each split's slice, pushed into rank 0's idle stage memory (fused RMSNorm)
-  float* s_push = reinterpret_cast<float*>(smem + C::kPushOff);   // [kMaxSplits][B]
   const float* peer[kMaxSplits];
 #pragma unroll
   for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? cluster.map_shared_rank(mine, q) : mine;
@@ -541,6 +553,7 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
         }
       }
     }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");   // this CTA read its peers
   } else {
     // slice of the tile's kRows rows in whole 4-row groups; unit = (slot, 4 rows); units
     // run rows fastest across threads, so y and the next operand are written in rows
@@ -602,9 +615,15 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
         }
         *reinterpret_cast<float4*>(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]) =
             make_float4(y[0], y[1], y[2], y[3]);
-        if (a.dec.kind) {
+        if (a.dec.kind) {   // the 4 rows' best first: one shared atomic per unit
+          unsigned long long k = 0ull;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) greedy_add(&s_best[bcol[i]], s_dflags, y[c], mrow[i] + c);
+          for (int c = 0; c < 4; ++c) {
+            if (mrow[i] + c >= a.M) break;
+            if (isnan(y[c])) s_dflags[0] = 1u;
+            else k = max(k, greedy_key(y[c], mrow[i] + c));
+          }
+          if (k) atomicMax(&s_best[bcol[i]], k);
         }
         if (norm_out) {
           uint16_t hi[4], lo[4];
@@ -627,7 +646,8 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
             *reinterpret_cast<float4*>(sq + off[i] - r0) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    if (norm_out) {   // this slice's sums of y^2, in row order, pushed to rank 0 of the tile
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");   // this CTA read its peers
+    if (norm_out) {   // this slice's sums of y^2, in row order: one partial per CTA
       __syncthreads();
       if (threadIdx.x < B) {
         float ss = 0.f;
@@ -638,16 +658,11 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
           ss += w.z;
           ss += w.w;
         }
-        cluster.map_shared_rank(s_push, 0)[sp * B + threadIdx.x] = ss;
+        a.ssq_out[((size_t)mt * S + sp) * B + threadIdx.x] = ss;
       }
     }
   }
-  cluster.sync();   // peers' partials are read and the pushed sums have landed in rank 0
-  if (norm_out && a.epi != EPI_SILU && sp == 0 && threadIdx.x < B) {
-    float ss = 0.f;   // one partial per tile: the slices added in split order
-    for (int q = 0; q < S; ++q) ss += s_push[q * B + threadIdx.x];
-    a.ssq_out[(size_t)mt * B + threadIdx.x] = ss;
-  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers done reading
   if (!ok && threadIdx.x == 0 && nkb > 0) atomicOr(a.status, PP_S_TIMEOUT);
   if (a.dec.kind) decide_tail(a, s_best, s_dflags, B);
 }

@@ -108,7 +108,8 @@ bool config_ok(const pp_config* c) {
   if (c->d_model % c->n_heads || !head_dim_ok(c->d_model / c->n_heads)) return false;
   if (c->dep_d <= 0 || c->dep_layers <= 0 || c->dep_heads <= 0 || c->dep_ffn <= 0) return false;
   if (c->dep_d % c->dep_heads || !head_dim_ok(c->dep_d / c->dep_heads)) return false;
-  if (c->dep_heads > 32) return false;  // one warp per depformer head in one CTA
+  // one warp per depformer head in one CTA, within the step attention's register budget
+  if (c->dep_heads > kDepAttnMaxHeads(c->dep_d / c->dep_heads)) return false;
   if (c->n_q != 16 || c->text_vocab <= 0 || c->audio_card <= 0) return false;
   if (c->window <= 0 || c->max_batch <= 0 || c->max_batch > kMaxBatch) return false;
   // 16-byte rows for the vectorised weight and activation streams
@@ -497,9 +498,9 @@ cudaError_t enqueue_user_steps_batched(const Group* e, cudaStream_t s, Prof* pro
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
   const int nb = kDepBatch, k0 = D.nq - kDepBatch;
-  const int p_din = mm[MM_BDIN].m_tiles;
-  const int p_do = mm[MM_BDO].m_tiles;
-  const int p_ddown = mm[MM_BDDOWN].m_tiles;
+  const int p_din = mm[MM_BDIN].m_tiles * mm[MM_BDIN].splits;
+  const int p_do = mm[MM_BDO].m_tiles * mm[MM_BDO].splits;
+  const int p_ddown = mm[MM_BDDOWN].m_tiles * mm[MM_BDDOWN].splits;
   const long long opd = 2LL * D.Bp * D.dd, opf = 2LL * D.Bp * D.Fd;
   const int R = 2 * D.Bp;
   {
@@ -630,12 +631,12 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   const Dims& D = e->D;
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
-  // fused-norm partials: one per M-tile of the producing contraction
-  const int p_o = mm[MM_O].m_tiles;
-  const int p_down = mm[MM_DOWN].m_tiles;
-  const int p_din = mm[MM_DIN].m_tiles;
-  const int p_do = mm[MM_DO].m_tiles;
-  const int p_ddown = mm[MM_DDOWN].m_tiles;
+  // fused-norm partials: one per CTA (M-tile x split) of the producing contraction
+  const int p_o = mm[MM_O].m_tiles * mm[MM_O].splits;
+  const int p_down = mm[MM_DOWN].m_tiles * mm[MM_DOWN].splits;
+  const int p_din = mm[MM_DIN].m_tiles * mm[MM_DIN].splits;
+  const int p_do = mm[MM_DO].m_tiles * mm[MM_DO].splits;
+  const int p_ddown = mm[MM_DDOWN].m_tiles * mm[MM_DDOWN].splits;
   MARK(PP_K_BEGIN);
   PP_TRY(launch_begin(D, b, b.attn_alpha, b.op_d, b.ssq, s));
   for (int l = 0; l < D.L; ++l) {

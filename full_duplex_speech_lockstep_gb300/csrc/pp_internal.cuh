@@ -124,6 +124,11 @@ struct Buffers {
   int* ppart_idx;          // [kPMaxGrid][kPMaxB]
 };
 
+// The depformer step attention runs one warp per head in one CTA; its register use
+// bounds the CTA to 512 threads (head dim 32 or 64) or 256 (head dim 128).
+constexpr int kDepAttnMaxThreads(int head_dim) { return head_dim == 128 ? 256 : 512; }
+constexpr int kDepAttnMaxHeads(int head_dim) { return kDepAttnMaxThreads(head_dim) / 32; }
+
 constexpr int kMaxUnits = 4096;      // cap on (M-tile x K-split) units of one contraction
 constexpr int kMaxSplits = 8;        // K-splits of one tile form one (portable) cluster
 constexpr int kMaxTiles = 1024;      // cap on M-tiles of one contraction
@@ -251,7 +256,8 @@ struct UmmaArgs {
   const int32_t* test_ctl;   // optional fault-test word (see pp_async.cuh)
   // Fused RMSNorm, producer side (EPI_ADD / EPI_EMB): besides y, write the next
   // contraction's operand hi/lo(norm_alpha * y) [2*Bp][M] and the sums of y^2 over each
-  // M-tile's rows, ssq_out[tile * B + b] (the splits of a tile are added in order).
+  // row slice: ssq_out[(tile * splits + split) * B + b], one partial per CTA (the slice
+  // of the tile's rows that CTA finalises; the whole tile when it is not split).
   const float* norm_alpha;
   uint16_t* norm_op;
   float* ssq_out;

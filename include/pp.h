@@ -68,7 +68,8 @@ typedef struct {
   int32_t n_q;           /* 16 audio rows = depformer steps (must be 16) */
   int32_t dep_d;         /* 1024 */
   int32_t dep_layers;    /* 6 */
-  int32_t dep_heads;     /* 16; head dim = dep_d / dep_heads, one of 32, 64, 128 */
+  int32_t dep_heads;     /* 16; head dim = dep_d / dep_heads, one of 32, 64, 128; at most
+                            16 heads (8 with head dim 128) */
   int32_t dep_ffn;       /* depformer FFN width */
   int32_t window;        /* 3000 ring positions per slot */
   int32_t max_batch;     /* slots, 1..64 */

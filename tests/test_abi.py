@@ -138,6 +138,21 @@ def test_fault_test_word_rejects_bad_arguments():
     assert lib.pp_test_faults(None, 0, 0, 0, None) == pp.PP_EINVAL
 
 
+def test_depformer_head_count_limit():
+    """The depformer step attention takes one warp per head in one CTA: at most 16 heads,
+    8 with head dim 128."""
+    import dataclasses
+    for dd, heads, good in [(1024, 16, True), (2048, 32, False), (1024, 8, True),
+                            (2048, 16, False), (4096, 32, False), (512, 16, True)]:
+        s = dataclasses.replace(synth.TINY, dep_d=dd, dep_heads=heads, dep_ffn=2 * dd)
+        cfg = pp.make_config(s, 4)
+        if good:
+            assert pp.pp_workspace_bytes(cfg) > 0, (dd, heads)
+        else:
+            with pytest.raises(pp.PPError):
+                pp.pp_workspace_bytes(cfg)
+
+
 def test_low_latency_config_limits():
     """The persistent depformer serves engines of at most 8 slots on the tensor-core path."""
     ok = pp.make_config(synth.TINY, 8, pp.PP_FLAG_LOW_LATENCY)
