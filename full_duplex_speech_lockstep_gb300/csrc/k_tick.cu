@@ -20,13 +20,6 @@ __device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
   }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  // round to nearest even, NaN kept quiet
-  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-  a = (a & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : a + 0x7FFFu + ((a >> 16) & 1u);
-  b = (b & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : b + 0x7FFFu + ((b >> 16) & 1u);
-  return (a >> 16) | (b & 0xFFFF0000u);
-}
 
 // Fixed-order block sum: per-warp butterfly, then warp 0 adds the warp totals in order.
 template <int NT>

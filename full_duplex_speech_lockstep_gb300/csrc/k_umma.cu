@@ -69,29 +69,52 @@ __device__ __forceinline__ void epi_store(const UmmaArgs& a, int b, int m, float
 // two halves share every activation tile (half the activation bytes per weight byte).
 // Order-preserving 64-bit key of a finite logit at a row: a larger value wins, then the
 // lower row (the greedy rule); -0 counts as +0.  Any reduction order gives the same max.
-__device__ __forceinline__ unsigned long long greedy_key(float v, int row) {
+// The high word (greedy_bits) is never 0 for a non-NaN value, infinities included.
+__device__ __forceinline__ uint32_t greedy_bits(float v) {
   if (v == 0.f) v = 0.f;
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// A warp's candidates, one logit per lane (valid: the lane holds one): the warp's
-// best key (the largest order bits, then the lowest row among the lanes that hold them)
-// goes to shared memory in one atomic instead of 32 colliding ones.  Every lane of the
-// warp calls it.
-__device__ __forceinline__ void greedy_add_warp(unsigned long long* best, unsigned* flags,
-                                                float v, bool valid, int row) {
-  uint32_t hi = 0u;   // 0: no candidate (finite values and infinities map above 0)
-  if (valid) {
-    if (isnan(v)) flags[0] = 1u;
-    else hi = (uint32_t)(greedy_key(v, row) >> 32);
+__device__ __forceinline__ unsigned long long greedy_key(float v, int row) {
+  return ((unsigned long long)greedy_bits(v) << 32) |
+         (unsigned long long)(0xFFFFFFFFu - (uint32_t)row);
+}
+
+// EPI_ROPE for 4 consecutive rows m..m+3 of open slot s (two RoPE pairs of one head; t:
+// cos, sin of both pairs; widx: the slot's ring row): the query (scaled) to q and q_op,
+// the key (rotated) and value to the ring.
+__device__ __forceinline__ void rope_store(const RopeArgs& r, int s, int m, const float* y,
+                                           float4 t, int widx) {
+  const int sec = m / r.d, w = m - sec * r.d, h = w / r.Dh, e = w - h * r.Dh;
+  const size_t blk = (size_t)r.W * r.Dh;
+  const size_t at = (size_t)widx * r.Dh + e;
+  uint16_t* ring = r.ring + (size_t)s * 2 * r.H * blk;
+  if (sec == 2) {
+    *reinterpret_cast<uint2*>(ring + (size_t)(r.H + h) * blk + at) =
+        make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+    return;
   }
-  const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, hi);
-  if (mx == 0u) return;
-  const uint32_t mr = __reduce_min_sync(0xFFFFFFFFu, hi == mx ? (uint32_t)row : 0xFFFFFFFFu);
-  if ((threadIdx.x & 31) == 0)
-    atomicMax(best, ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - mr));
+  float o[4] = {y[0] * t.x - y[1] * t.y, y[0] * t.y + y[1] * t.x,
+                y[2] * t.z - y[3] * t.w, y[2] * t.w + y[3] * t.z};
+  if (sec == 1) {
+    *reinterpret_cast<uint2*>(ring + (size_t)h * blk + at) =
+        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+    return;
+  }
+  const float qs = 1.4426950408889634f / sqrtf((float)r.Dh);
+  uint16_t hi[4], lo[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    o[c] *= qs;
+    bf16_split(o[c], hi[c], lo[c]);
+  }
+  *reinterpret_cast<float4*>(r.q + (size_t)s * r.d + w) = make_float4(o[0], o[1], o[2], o[3]);
+  uint16_t* qo = r.q_op + (size_t)(s * r.H + h) * 2 * r.Dh + e;
+  *reinterpret_cast<uint2*>(qo) = make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16),
+                                             (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+  *reinterpret_cast<uint2*>(qo + r.Dh) = make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16),
+                                                    (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
 }
 
 // The fused greedy decision of a head contraction: each CTA folds its per-slot keys
@@ -199,6 +222,7 @@ struct Cfg {
   // fused greedy decision: [64] keys and 2 flags after the partials
   static constexpr int kKeyOff = ((2 * (N / 2) * kPR * 4) + 1023) / 1024 * 1024;
   static_assert(kKeyOff + 64 * 8 + 16 <= kStages * kStageBytes, "decision keys");
+  static_assert((N / 2) * (kRows + 1) * 4 <= kKeyOff, "slot-major logits of a head tile");
   // single split: SiLU exchange [kPairs][N/2] and y^2 [kRows][N/2 + 1] in the stages
   static_assert(kRows * (N / 2 + 1) * 4 <= kStages * kStageBytes, "y^2 area");
   static_assert(kStages >= 2, "pipeline depth");
@@ -455,10 +479,35 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
         for (int b = 0; b < N / 2; ++b)
           if (b < B) epi_store(a, b, m, acc[b]);
       }
-      if (a.dec.kind) {   // every lane of every warp is here (ok is uniform)
+      if (a.dec.kind) {
+        // the tile's logits slot-major in the idle stages, then one warp per slot: a short
+        // rolled loop (this runs once per launch, from a cold instruction cache)
+        constexpr int XL = C::kRows + 1;
+        float* xs = reinterpret_cast<float*>(smem);   // [N/2][XL]
 #pragma unroll
         for (int b = 0; b < N / 2; ++b)
-          if (b < B) greedy_add_warp(&s_best[b], s_dflags, acc[b], row_ok, m);
+          if (b < B) xs[b * XL + tr] = acc[b];
+        __syncthreads();
+        const int rows = min(C::kRows, a.M - mt * C::kRows);
+#pragma unroll 1
+        for (int b = warp; b < B; b += C::kThreads / 32) {
+          uint32_t hi = 0u, row = 0u;   // rows visited in ascending order: ties keep the first
+#pragma unroll 1
+          for (int q = lane; q < rows; q += 32) {
+            const float v = xs[b * XL + q];
+            if (isnan(v)) {
+              s_dflags[0] = 1u;
+            } else {
+              const uint32_t h = greedy_bits(v);
+              if (h > hi) { hi = h; row = (uint32_t)q; }
+            }
+          }
+          const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, hi);
+          const uint32_t mr = __reduce_min_sync(0xFFFFFFFFu, hi == mx ? row : 0xFFFFFFFFu);
+          if (lane == 0 && mx)
+            s_best[b] = ((unsigned long long)mx << 32) |
+                        (unsigned long long)(0xFFFFFFFFu - (uint32_t)(mt * C::kRows + mr));
+        }
         decide_tail(a, s_best, s_dflags, B);
       }
       return;
@@ -500,6 +549,12 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
 #pragma unroll
   for (int b = 0; b < N / 2; ++b)
     if (b < B) mine[b * PR + tr] = ok ? acc[b] : 0.f;
+  // EPI_ROPE: each slot's open flag and ring row, staged once (the key area is unused)
+  int* s_rope = reinterpret_cast<int*>(smem + C::kKeyOff);   // [2][64]
+  if (a.epi == EPI_ROPE && threadIdx.x < B) {
+    s_rope[threadIdx.x] = a.rope.live[threadIdx.x];
+    s_rope[64 + threadIdx.x] = a.rope.pos[threadIdx.x] % a.rope.W;
+  }
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   const int S = a.splits;
@@ -586,6 +641,10 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
                                 __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
           }
           if (norm_out) al[i] = ld4(a.norm_alpha + mrow[i]);
+          if (a.epi == EPI_ROPE && mrow[i] < 2 * a.rope.d) {   // q, k: cos, sin of 2 pairs
+            const int w = mrow[i] % a.rope.d;
+            al[i] = ld4(a.rope.cs + (size_t)bcol[i] * a.rope.Dh + w % a.rope.Dh);
+          }
         }
       }
       float4 pv[CH][kMaxSplits];
@@ -613,8 +672,11 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
           if (norm_in) vv *= rs;
           y[c] = vv + exv[c];
         }
-        *reinterpret_cast<float4*>(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]) =
-            make_float4(y[0], y[1], y[2], y[3]);
+        if (a.epi == EPI_ROPE) {
+          if (s_rope[bcol[i]]) rope_store(a.rope, bcol[i], mrow[i], y, al[i], s_rope[64 + bcol[i]]);
+        } else
+          *reinterpret_cast<float4*>(a.Y + (size_t)bcol[i] * a.ldy + mrow[i]) =
+              make_float4(y[0], y[1], y[2], y[3]);
         if (a.dec.kind) {   // the 4 rows' best first: one shared atomic per unit
           unsigned long long k = 0ull;
 #pragma unroll

@@ -439,9 +439,10 @@ struct Chunks {
 cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, int epi, float* Y,
                       int ldy, const uint16_t* emb, uint16_t* op_out, int ld_op, cudaStream_t s,
                       const NormIO& nio = NormIO(), const Chunks& ch = Chunks(),
-                      const DecideArgs* dec = nullptr) {
+                      const DecideArgs* dec = nullptr, const RopeArgs* rope = nullptr) {
   UmmaArgs a{};
   if (dec) a.dec = *dec;
+  if (rope) a.rope = *rope;
   a.halves = g.H;
   a.chunks = ch.n;
   a.a_chunk_rows = ch.a_rows;
@@ -594,6 +595,22 @@ cudaError_t enqueue_user_steps_batched(const Group* e, cudaStream_t s, Prof* pro
                    chd);
 }
 
+// The temporal layer `l`'s RoPE and ring append, for the qkv contraction's epilogue.
+RopeArgs rope_args(const Dims& D, const Buffers& b, int l) {
+  RopeArgs r{};
+  r.live = b.live;
+  r.pos = b.pos;
+  r.cs = b.rope_cs;
+  r.q = b.q;
+  r.q_op = b.q_op;
+  r.ring = b.ring + (size_t)l * D.B * 2 * D.H * D.W * D.Dh;
+  r.d = D.d;
+  r.H = D.H;
+  r.Dh = D.Dh;
+  r.W = D.W;
+  return r;
+}
+
 // The fused greedy decision of a head launch (kind 1: text row 0; kind 2: depformer step
 // `step`).
 bool make_decide(const Dims& D, const Buffers& b, const Mm& g, int kind, int step,
@@ -637,6 +654,8 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   const int p_din = mm[MM_DIN].m_tiles * mm[MM_DIN].splits;
   const int p_do = mm[MM_DO].m_tiles * mm[MM_DO].splits;
   const int p_ddown = mm[MM_DDOWN].m_tiles * mm[MM_DDOWN].splits;
+  // the K-split epilogue finalises whole 4-row groups of one slot, i.e. two RoPE pairs
+  const bool rope_fused = mm[MM_QKV].splits > 1;
   MARK(PP_K_BEGIN);
   PP_TRY(launch_begin(D, b, b.attn_alpha, b.op_d, b.ssq, s));
   for (int l = 0; l < D.L; ++l) {
@@ -645,9 +664,16 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     qn.nparts = (l == 0) ? 1 : p_down;
     qn.K = D.d;
     MARK(PP_K_QKV);
-    PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_STORE, b.qkv, 3 * D.d, nullptr, nullptr, 0, s, qn));
-    MARK(PP_K_ROPE_RING);
-    PP_TRY(launch_rope_ring(D, b, l, s));
+    if (rope_fused) {   // RoPE and the ring append in the contraction's epilogue
+      RopeArgs ra = rope_args(D, b, l);
+      PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_ROPE, nullptr, 0, nullptr, nullptr, 0,
+                       s, qn, Chunks(), nullptr, &ra));
+    } else {
+      PP_TRY(mm_launch(D, b, mm[MM_QKV], l * 3 * D.d, EPI_STORE, b.qkv, 3 * D.d, nullptr, nullptr,
+                       0, s, qn));
+      MARK(PP_K_ROPE_RING);
+      PP_TRY(launch_rope_ring(D, b, l, s));
+    }
     MARK(PP_K_ATTN);
     PP_TRY(launch_attn(D, b, l, true, e->has_amaps ? &e->amaps : nullptr, s));
     NormIO on;

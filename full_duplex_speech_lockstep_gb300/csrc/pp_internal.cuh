@@ -190,6 +190,15 @@ cudaError_t launch_begin(const Dims& D, const Buffers& b, const float* alpha, ui
 cudaError_t launch_rmsnorm(const Dims& D, const float* x, int ldx, const float* alpha, int K,
                            float* out, int ldo, uint16_t* op, cudaStream_t s);
 
+// two values as packed bf16 (lo in the low half)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  // round to nearest even, NaN kept quiet
+  uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
+  a = (a & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : a + 0x7FFFu + ((a >> 16) & 1u);
+  b = (b & 0x7FFFFFFFu) > 0x7F800000u ? 0x7FC00000u : b + 0x7FFFu + ((b >> 16) & 1u);
+  return (a >> 16) | (b & 0xFFFF0000u);
+}
+
 // hi = bf16(v) and lo = bf16(v - hi), both rounded to nearest even (NaN stays NaN)
 __device__ __forceinline__ void bf16_split(float v, uint16_t& hi, uint16_t& lo) {
   uint32_t u = __float_as_uint(v);
@@ -234,8 +243,19 @@ struct DecideArgs {
 };
 
 // Tensor-core contraction (k_umma.cu).
+struct RopeArgs {
+  const int32_t* live;     // [B]
+  const int32_t* pos;      // [B]
+  const float* cs;         // [B][Dh/2][2] cos, sin of this tick's position
+  float* q;                // [B][d] rotated query x log2(e)/sqrt(Dh)
+  uint16_t* q_op;          // [B][H][2][Dh] the same as bf16 hi/lo rows
+  uint16_t* ring;          // this layer's ring [B][2][H][W][Dh] bf16
+  int d, H, Dh, W;
+};
+
 struct UmmaArgs {
   int halves;          // 128-row halves of the weight tile: 1 or 2 (a function of the shape)
+  RopeArgs rope;       // EPI_ROPE
   int M;               // output rows (EPI_SILU: number of gate/up pairs)
   int pair_rows;       // EPI_SILU: F, the up rows start pair_rows after the gate rows; else 0
   int row0;            // first row of this matrix in the stacked weight tensor map
@@ -289,7 +309,10 @@ cudaError_t launch_umma(const UmmaArgs& a, const CUtensorMap& mA, const CUtensor
                         cudaStream_t s);
 cudaError_t umma_setup(int N);
 
-enum GemvEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_EMB = 3 };
+// EPI_ROPE (tensor-core path only): the temporal qkv contraction's rows are not stored;
+// q and k are rotated at the slot's position (interleaved pairs), the scaled query goes
+// to q / q_op and k, v are appended to the layer's ring as bf16, for open slots only.
+enum GemvEpi { EPI_STORE = 0, EPI_ADD = 1, EPI_SILU = 2, EPI_EMB = 3, EPI_ROPE = 4 };
 struct GemvArgs {
   const uint16_t* W;     // [M, K] bf16 (EPI_SILU: [2M, K], gate rows then up rows)
   int M, K;

@@ -168,3 +168,46 @@ def test_isolation_full_shape_attention_merge_paths():
         e1.close_engine()
         assert np.array_equal(bc[:, s], ac[:, 0]), ("columns differ", s)
         assert np.array_equal(bl[:, s].view(np.uint32), al[:, 0].view(np.uint32)), ("logits", s)
+
+
+@pytest.mark.parametrize("path", ["tensor", "cuda_core"])
+def test_ring_append_touches_only_open_slots_at_their_position(path):
+    """Each tick appends a slot's k and v to its ring at position pos mod W, for open slots
+    only (on the tensor-core path this happens in the qkv contraction's epilogue, on the
+    CUDA-core path in a separate kernel): a closed slot's blocks keep every byte, an open
+    slot's blocks change in the row of its position and nowhere else."""
+    import torch
+    import full_duplex_speech_lockstep_gb300 as pp
+    from harness import device_view
+    s = synth.SMALL
+    B, L, H, W, Dh = 4, s.n_layers, s.n_heads, s.window, s.head_dim
+    flags = pp.PP_FLAG_CUDA_CORE_GEMM if path == "cuda_core" else 0
+    eng = pp.Engine(s, B, device_weights(synth.make_weights_host(s, 61)), flags=flags)
+    blocks = {(l, b, kv): device_view(eng.ring_block(l, b, kv), H * W * Dh).view(H, W, Dh)
+              for l in range(L) for b in range(B) for kv in range(2)}
+    for v in blocks.values():
+        v.fill_(0x1234)
+    torch.cuda.synchronize()
+    user = synth.uniform_i32(6 * B * 8, 62, 0, 0, s.audio_card).reshape(6, B, 8)
+    prev = torch.from_numpy(np.tile(initial_column(s), (B, 1))).cuda()
+    eng.open(0)
+    for t in range(6):
+        if t == 2:
+            eng.open(2)
+            prev[2] = torch.from_numpy(initial_column(s)).cuda()   # not the closed-slot -1s
+        live = [0] if t < 2 else [0, 2]
+        pos = {b: eng.pos(b) for b in live}
+        before = {k: v.clone() for k, v in blocks.items()}
+        prev = eng.step(prev, torch.from_numpy(user[t]).cuda()).clone()
+        torch.cuda.synchronize()
+        for (l, b, kv), v in blocks.items():
+            if b not in live:
+                assert torch.equal(v, before[(l, b, kv)]), (t, l, b, kv)
+                continue
+            p = pos[b] % W
+            rows = torch.ones(W, dtype=torch.bool, device="cuda")
+            rows[p] = False
+            assert torch.equal(v[:, rows], before[(l, b, kv)][:, rows]), (t, l, b, kv)
+            assert (v[:, p] != before[(l, b, kv)][:, p]).any(dim=1).all(), (t, l, b, kv)
+    assert eng.status() == 0
+    eng.close_engine()
