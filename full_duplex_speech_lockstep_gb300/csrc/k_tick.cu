@@ -470,30 +470,32 @@ cudaError_t launch_dep_attn(const Dims& D, const Buffers& b, int step, int layer
 
 // ---- the batched user steps -------------------------------------------------------------
 // Steps 8..15 of a frame take known tokens (row 8, then the user codes), so they run as one
-// pass: for each slot and head this stores the k, v of every batched step at its step
-// index of the frame's cache, then step 8 + c attends over steps 0..8+c with the same
-// arithmetic, in the same order, as the one-step kernel above.
+// pass.  One CTA per (slot, step 8 + c), one warp per head: step 8 + c attends over steps
+// 0..8+c with the same arithmetic, in the same order, as the one-step kernel above.  The
+// keys and values of steps 0..7 come from the frame's cache, those of steps 8..8+c
+// straight from this pass's qkv rows.  Nothing reads cache rows 8..15 within the frame, and
+// the next frame overwrites the cache from step 0, so this pass appends nothing.
 template <int E>  // head dim / 32
-__global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E)) k_dep_attn_b(Dims D, Buffers b, int layer) {
+__global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E))
+k_dep_attn_b(Dims D, Buffers b, int layer) {
   pdl_wait_and_trigger();
-  const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.x, c = blockIdx.y, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
-  const int k0 = D.nq - kDepBatch;
-  const size_t op_chunk = (size_t)2 * D.Bp * D.dd;
+  const int k0 = D.nq - kDepBatch, step = k0 + c;
+  uint16_t* op = b.op_dob + (size_t)c * 2 * D.Bp * D.dd;
+  float* out = b.dout_b + ((size_t)c * D.B + s) * D.dd;
   if (!b.live[s]) {
-    for (int c = 0; c < kDepBatch; ++c)
-      for (int e = 0; e < E; ++e) {
-        const int i = h * D.Dhd + lane + 32 * e;
-        b.dout_b[((size_t)c * D.B + s) * D.dd + i] = 0.f;
-        op_store(b.op_dob + c * op_chunk, D.dd, D.Bp, s, i, 0.f);
-      }
+    for (int e = 0; e < E; ++e) {
+      const int i = h * D.Dhd + lane + 32 * e;
+      out[i] = 0.f;
+      op_store(op, D.dd, D.Bp, s, i, 0.f);
+    }
     return;
   }
-  float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
-  // every step of the frame in registers, this lane's dims of this head: steps 0..k0-1
-  // from the cache, steps k0.. and the queries from this pass's qkv rows, all loaded
-  // before the cache append (a store between them would order the later loads after it)
-  float kc[16][E], vc[16][E], qb[kDepBatch][E];
+  const float* cache = b.dkv + ((size_t)s * D.Ld + layer) * D.nq * 2 * D.dd;
+  // this lane's dims of this head: steps 0..k0-1 from the cache, k0..step and the query
+  // from this pass's qkv rows, all loaded at once
+  float kc[16][E], vc[16][E], q[E];
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
     if (t >= k0) break;
@@ -504,70 +506,109 @@ __global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E)) k_dep_attn_b(Dims 
     }
   }
 #pragma unroll
-  for (int c = 0; c < kDepBatch; ++c) {
-    const float* row = b.dqkv_b + ((size_t)c * D.B + s) * 3 * D.dd + h * D.Dhd;
+  for (int c2 = 0; c2 < kDepBatch; ++c2) {
+    if (c2 > c) break;
+    const float* row = b.dqkv_b + ((size_t)c2 * D.B + s) * 3 * D.dd + h * D.Dhd;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      qb[c][e] = row[lane + 32 * e];
-      kc[16 - kDepBatch + c][e] = row[D.dd + lane + 32 * e];
-      vc[16 - kDepBatch + c][e] = row[2 * D.dd + lane + 32 * e];
+      kc[16 - kDepBatch + c2][e] = row[D.dd + lane + 32 * e];
+      vc[16 - kDepBatch + c2][e] = row[2 * D.dd + lane + 32 * e];
+      if (c2 == c) q[e] = row[lane + 32 * e];
     }
   }
-#pragma unroll
-  for (int c = 0; c < kDepBatch; ++c)
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      cache[(size_t)(k0 + c) * 2 * D.dd + h * D.Dhd + lane + 32 * e] = kc[16 - kDepBatch + c][e];
-      cache[(size_t)(k0 + c) * 2 * D.dd + D.dd + h * D.Dhd + lane + 32 * e] =
-          vc[16 - kDepBatch + c][e];
-    }
   const float scale = 1.0f / sqrtf((float)D.Dhd);
+  float sc[16];
+  float m = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < kDepBatch; ++c) {
-    const int step = k0 + c;
-    const float* q = qb[c];
-    float sc[16];
-    float m = -INFINITY;
+  for (int t = 0; t < 16; ++t) {
+    if (t > step) break;
+    float dot = 0.f;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      if (t > step) break;
-      float dot = 0.f;
+    for (int e = 0; e < E; ++e) dot = fmaf(q[e], kc[t][e], dot);
 #pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(q[e], kc[t][e], dot);
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    sc[t] = dot * scale;
+    m = fmaxf(m, sc[t]);
+  }
+  float l = 0.f, acc[E];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      sc[t] = dot * scale;
-      m = fmaxf(m, sc[t]);
-    }
-    float l = 0.f, acc[E];
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int t = 0; t < 16; ++t) {
+    if (t > step) break;
+    const float p = expf(sc[t] - m);
+    l += p;
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      if (t > step) break;
-      const float p = expf(sc[t] - m);
-      l += p;
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vc[t][e], acc[e]);
+  }
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, vc[t][e], acc[e]);
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float v = acc[e] / l;
-      const int i = h * D.Dhd + lane + 32 * e;
-      b.dout_b[((size_t)c * D.B + s) * D.dd + i] = v;
-      op_store(b.op_dob + c * op_chunk, D.dd, D.Bp, s, i, v);
-    }
+  for (int e = 0; e < E; ++e) {
+    const float v = acc[e] / l;
+    const int i = h * D.Dhd + lane + 32 * e;
+    out[i] = v;
+    op_store(op, D.dd, D.Bp, s, i, v);
   }
 }
 
 cudaError_t launch_dep_attn_batch(const Dims& D, const Buffers& b, int layer, cudaStream_t s) {
   const int threads = D.Hd * 32;
+  const dim3 grid(D.B, kDepBatch);
   switch (D.Dhd) {
-    case 32: return launch_k(k_dep_attn_b<1>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
-    case 64: return launch_k(k_dep_attn_b<2>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
-    case 128: return launch_k(k_dep_attn_b<4>, dim3(D.B), dim3(threads), 0, s, 1, D, b, layer);
+    case 32: return launch_k(k_dep_attn_b<1>, grid, dim3(threads), 0, s, 1, D, b, layer);
+    case 64: return launch_k(k_dep_attn_b<2>, grid, dim3(threads), 0, s, 1, D, b, layer);
+    case 128: return launch_k(k_dep_attn_b<4>, grid, dim3(threads), 0, s, 1, D, b, layer);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// ---- depformer step input from the all-steps in-projection ------------------------------
+// One CTA per slot and step chunk: y = P_k z (this tick's contraction of all 16 steps'
+// in-projections, pz[B][nq * dd], scaled by the final norm) + D_k[tok_k] (bf16 table row),
+// the first layer's normalised operand (alpha * y as bf16 hi/lo) and the slot's sum of y^2
+// (one partial: dims in thread order, then a fixed-order block sum).  Chunk c (grid.y)
+// is step k0 + c, with its token table tok + c * B and output strides as given.
+__global__ void __launch_bounds__(256) k_dep_in(Dims D, Buffers b, int k0, const int32_t* tok,
+                                                const uint16_t* emb, long long emb_chunk,
+                                                float* y, long long y_chunk, uint16_t* op,
+                                                long long op_chunk, float* ssq) {
+  __shared__ float sh[9];
+  pdl_wait_and_trigger();
+  const int s = blockIdx.x, c = blockIdx.y, k = k0 + c;
+  const int t = tok[(size_t)c * D.B + s];
+  const float* pz = b.pz + (size_t)s * D.nq * D.dd + (size_t)k * D.dd;
+  const uint16_t* e = emb + c * emb_chunk + (size_t)t * D.dd;
+  float* yo = y + c * y_chunk + (size_t)s * D.dd;
+  uint16_t* opc = op + c * op_chunk;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 4; i < D.dd; i += 256 * 4) {
+    const float4 p = *reinterpret_cast<const float4*>(pz + i);
+    const uint2 w = *reinterpret_cast<const uint2*>(e + i);
+    const float v[4] = {p.x + __uint_as_float(w.x << 16), p.y + __uint_as_float(w.x & 0xFFFF0000u),
+                        p.z + __uint_as_float(w.y << 16), p.w + __uint_as_float(w.y & 0xFFFF0000u)};
+    *reinterpret_cast<float4*>(yo + i) = make_float4(v[0], v[1], v[2], v[3]);
+    const float4 al = *reinterpret_cast<const float4*>(b.dep_attn_alpha + i);
+    const float av[4] = {al.x, al.y, al.z, al.w};
+    uint16_t hi[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      bf16_split(av[q] * v[q], hi[q], lo[q]);
+      ss += v[q] * v[q];
+    }
+    *reinterpret_cast<uint2*>(opc + (size_t)s * D.dd + i) =
+        make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+    *reinterpret_cast<uint2*>(opc + (size_t)(D.Bp + s) * D.dd + i) =
+        make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+  }
+  ss = block_sum<256>(ss, sh);
+  if (threadIdx.x == 0) ssq[(size_t)c * D.B + s] = ss;
+}
+
+cudaError_t launch_dep_in(const Dims& D, const Buffers& b, int k0, int chunks, const int32_t* tok,
+                          const uint16_t* emb, long long emb_chunk, float* y, long long y_chunk,
+                          uint16_t* op, long long op_chunk, cudaStream_t s) {
+  if (D.dd % 4) return cudaErrorInvalidValue;
+  return launch_k(k_dep_in, dim3(D.B, chunks), dim3(256), 0, s, 1, D, b, k0, tok, emb, emb_chunk,
+                  y, y_chunk, op, op_chunk, b.ssq);
 }
 
 // Rows 9..16 straight from this frame's user codes (when depformer steps 8..15, whose

@@ -49,7 +49,7 @@ struct Mm {
 enum MmKind { MM_QKV, MM_O, MM_GU, MM_DOWN, MM_TEXT, MM_DIN, MM_DQKV, MM_DO, MM_DGU, MM_DDOWN,
               MM_DHEAD,
               // the depformer's batched user steps: one chunk of operand rows per step
-              MM_BDIN, MM_BDQKV, MM_BDO, MM_BDGU, MM_BDDOWN, MM_BDHEAD, MM_COUNT };
+              MM_BDQKV, MM_BDO, MM_BDGU, MM_BDDOWN, MM_BDHEAD, MM_COUNT };
 
 constexpr int kMaxGroups = 2;
 
@@ -234,6 +234,7 @@ size_t carve(const pp_config* c, char* base, Buffers* shared, Group* grp) {
     b.dh = cv.take<float>(Bs * D.Fd);
     b.tokb = cv.take<int32_t>(kDepBatch * Bs);
     b.y_b = cv.take<float>(kDepBatch * Bs * D.dd);
+    b.pz = cv.take<float>(Bs * D.nq * D.dd);
     b.dqkv_b = cv.take<float>(kDepBatch * Bs * 3 * D.dd);
     b.dout_b = cv.take<float>(kDepBatch * Bs * D.dd);
     const size_t R = 2 * (size_t)D.Bp;
@@ -391,7 +392,12 @@ bool plan_all(Group* e, int nsm) {
   ok &= plan_mm(&e->mm[MM_GU], b.wgu, D.L * 2 * D.F, D.F, D.d, D.F, b.op_d, Bp, nsm, 1, 1, Ht);
   ok &= plan_mm(&e->mm[MM_DOWN], b.wdown, D.L * D.d, D.d, D.F, 0, b.op_f, Bp, nsm, 1, 1, Ht);
   ok &= plan_mm(&e->mm[MM_TEXT], b.wtext, D.Vt, D.Vt, D.d, 0, b.op_z, Bp, nsm, 1, 1, Ht);
-  ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, nsm);
+  // every step's in-projection that the tick runs, in one launch (they read only this
+  // tick's z); none for the persistent depformer, which does its own
+  const int din_steps = D.dep_batched ? D.nq : D.dep_steps;
+  if (din_steps > 0)
+    ok &= plan_mm(&e->mm[MM_DIN], b.dep_inproj, D.nq * D.dd, din_steps * D.dd, D.d, 0, b.op_z,
+                  Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_dd, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_do, Bp, nsm);
   ok &= plan_mm(&e->mm[MM_DGU], b.dep_wgu, D.Ld * 2 * D.Fd, D.Fd, D.dd, D.Fd, b.op_dd, Bp, nsm);
@@ -399,7 +405,6 @@ bool plan_all(Group* e, int nsm) {
   ok &= plan_mm(&e->mm[MM_DHEAD], b.dep_heads, D.nq * D.Va, D.Va, D.dd, 0, b.op_dd, Bp, nsm);
   if (D.dep_batched) {
     const int nb = kDepBatch;
-    ok &= plan_mm(&e->mm[MM_BDIN], b.dep_inproj, D.nq * D.dd, D.dd, D.d, 0, b.op_z, Bp, nsm, nb, 1);
     ok &= plan_mm(&e->mm[MM_BDQKV], b.dep_wqkv, D.Ld * 3 * D.dd, 3 * D.dd, D.dd, 0, b.op_ddb, Bp,
                   nsm, nb, nb);
     ok &= plan_mm(&e->mm[MM_BDO], b.dep_wo, D.Ld * D.dd, D.dd, D.dd, 0, b.op_dob, Bp, nsm, nb, nb);
@@ -499,31 +504,17 @@ cudaError_t enqueue_user_steps_batched(const Group* e, cudaStream_t s, Prof* pro
   const Buffers& b = e->buf;
   const Mm* mm = e->mm;
   const int nb = kDepBatch, k0 = D.nq - kDepBatch;
-  const int p_din = mm[MM_BDIN].m_tiles * mm[MM_BDIN].splits;
+  const int p_din = 1;   // k_dep_in: one sum of y^2 per slot and step
   const int p_do = mm[MM_BDO].m_tiles * mm[MM_BDO].splits;
   const int p_ddown = mm[MM_BDDOWN].m_tiles * mm[MM_BDDOWN].splits;
   const long long opd = 2LL * D.Bp * D.dd, opf = 2LL * D.Bp * D.Fd;
   const int R = 2 * D.Bp;
-  {
-    NormIO in;
-    in.rstd_in = b.rstd_z;
-    in.alpha_out = b.dep_attn_alpha;
-    in.op_next = b.op_ddb;
-    in.ssq_out = b.ssq;
-    Chunks ch;
-    ch.n = nb;
-    ch.a_rows = D.dd;                      // in-projection P_{8+c}
-    ch.y = (long long)D.B * D.dd;
-    ch.op = opd;
-    ch.ssq_out = p_din * D.B;
-    ch.emb = (long long)(D.Va + 1) * D.dd; // audio table 8 + c - 1
-    ch.tok = D.B;
-    ch.tok_ptr = b.tokb;
-    MARK(PP_K_DEP_INPROJ);
-    PP_TRY(mm_launch(D, b, mm[MM_BDIN], k0 * D.dd, EPI_EMB, b.y_b, D.dd,
-                     b.dep_emb_audio + (size_t)(k0 - 1) * (D.Va + 1) * D.dd, nullptr, 0, s, in,
-                     ch));
-  }
+  // inputs of steps 8..15: P_{8+c} z (this tick's all-steps in-projection) + the audio
+  // table 8 + c - 1 at the chunk's token
+  MARK(PP_K_DEP_INPROJ);
+  PP_TRY(launch_dep_in(D, b, k0, nb, b.tokb, b.dep_emb_audio + (size_t)(k0 - 1) * (D.Va + 1) * D.dd,
+                       (long long)(D.Va + 1) * D.dd, b.y_b, (long long)D.B * D.dd, b.op_ddb, opd,
+                       s));
   for (int j = 0; j < D.Ld; ++j) {
     NormIO qn;
     qn.ssq_in = b.ssq;
@@ -651,7 +642,6 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   // fused-norm partials: one per CTA (M-tile x split) of the producing contraction
   const int p_o = mm[MM_O].m_tiles * mm[MM_O].splits;
   const int p_down = mm[MM_DOWN].m_tiles * mm[MM_DOWN].splits;
-  const int p_din = mm[MM_DIN].m_tiles * mm[MM_DIN].splits;
   const int p_do = mm[MM_DO].m_tiles * mm[MM_DO].splits;
   const int p_ddown = mm[MM_DDOWN].m_tiles * mm[MM_DDOWN].splits;
   // the K-split epilogue finalises whole 4-row groups of one slot, i.e. two RoPE pairs
@@ -701,7 +691,18 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
     tn.ssq_in = b.ssq;
     tn.nparts = p_down;
     tn.K = D.d;
-    tn.rstd_out = b.rstd_z;     // kept for the 16 depformer input projections
+    tn.rstd_out = b.rstd_z;     // kept for the persistent depformer's input projections
+    if (D.dep_steps > 0 || D.dep_batched) {
+      // every depformer step's in-projection P_k z at once: it reads only z, so it runs
+      // before the text head decides the first token; each step adds its token's row
+      NormIO pn;
+      pn.ssq_in = b.ssq;
+      pn.nparts = p_down;
+      pn.K = D.d;
+      MARK(PP_K_DEP_INPROJ);
+      PP_TRY(mm_launch(D, b, mm[MM_DIN], 0, EPI_STORE, b.pz, D.nq * D.dd, nullptr, nullptr, 0, s,
+                       pn));
+    }
     DecideArgs dt;
     const bool fuse = greedy && make_decide(D, b, mm[MM_TEXT], 1, 0, &dt);
     MARK(PP_K_TEXT_HEAD);
@@ -729,17 +730,12 @@ cudaError_t enqueue_tick_tensor(const Group* e, int dep_priority, cudaStream_t s
   for (int k = 0; k < D.dep_steps; ++k) {
     const uint16_t* emb =
         (k == 0) ? b.dep_emb_text : b.dep_emb_audio + (size_t)(k - 1) * (D.Va + 1) * D.dd;
-    NormIO in;
-    in.rstd_in = b.rstd_z;
-    in.alpha_out = b.dep_attn_alpha;
-    in.op_next = b.op_dd;
-    in.ssq_out = b.ssq;
     MARK(PP_K_DEP_INPROJ);
-    PP_TRY(mm_launch(D, b, mm[MM_DIN], k * D.dd, EPI_EMB, b.y, D.dd, emb, nullptr, 0, s, in));
+    PP_TRY(launch_dep_in(D, b, k, 1, b.tok, emb, 0, b.y, 0, b.op_dd, 0, s));
     for (int j = 0; j < D.Ld; ++j) {
       NormIO qn;
       qn.ssq_in = b.ssq;
-      qn.nparts = (j == 0) ? p_din : p_ddown;
+      qn.nparts = (j == 0) ? 1 : p_ddown;   // k_dep_in: one partial per slot
       qn.K = D.dd;
       MARK(PP_K_DEP_QKV);
       PP_TRY(mm_launch(D, b, mm[MM_DQKV], j * 3 * D.dd, EPI_STORE, b.dqkv, 3 * D.dd, nullptr,

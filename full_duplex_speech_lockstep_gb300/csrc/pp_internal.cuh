@@ -100,6 +100,7 @@ struct Buffers {
   // the depformer's batched user steps (steps 8..15, chunk c = step 8 + c)
   int32_t* tokb;           // [8][B] token feeding step 8 + c
   float* y_b;              // [8][B][dd]
+  float* pz;               // [B][nq * dd] every step's in-projection of this tick's z
   float* dqkv_b;           // [8][B][3dd]
   float* dout_b;           // [8][B][dd]
   // bf16 hi/lo activation operands of the tensor-core contractions, [2*Bp][K]
@@ -390,6 +391,11 @@ cudaError_t launch_dep_persist(const PersistArgs& p, cudaStream_t s);
 
 // attention of the batched user steps of one depformer layer
 cudaError_t launch_dep_attn_batch(const Dims& D, const Buffers& b, int layer, cudaStream_t s);
+// Depformer input of `chunks` consecutive steps from k0 (b.pz + the token tables): y, the
+// first layer's operand and one sum of y^2 per slot and step (b.ssq[c * B + s]).
+cudaError_t launch_dep_in(const Dims& D, const Buffers& b, int k0, int chunks, const int32_t* tok,
+                          const uint16_t* emb, long long emb_chunk, float* y, long long y_chunk,
+                          uint16_t* op, long long op_chunk, cudaStream_t s);
 constexpr int kDepBatch = 8;   // user steps run as one batched pass (n_q / 2)
 cudaError_t sample_setup(const Dims& D);   // shared-memory opt-in of the decision kernels
 cudaError_t launch_sample_rows(const float* logits, int64_t ld, int rows, int n, float temperature,
