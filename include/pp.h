@@ -329,14 +329,15 @@ int pp_test_faults(pp_engine* e, int32_t wait_polls, int32_t withhold, int32_t k
 enum pp_kernel_kind {
   PP_K_BEGIN = 0,   /* control + 17-table embedding sum + RoPE angle table */
   PP_K_NORM,        /* RMSNorm of the temporal stream */
-  PP_K_QKV,         /* fused QKV in-projection */
-  PP_K_ROPE_RING,   /* RoPE + ring-KV write */
+  PP_K_QKV,         /* fused QKV in-projection (tensor-core path: with RoPE + ring-KV write) */
+  PP_K_ROPE_RING,   /* RoPE + ring-KV write (CUDA-core path) */
   PP_K_ATTN,        /* split-K sliding-window ring attention (+ chunk merge) */
   PP_K_OPROJ,       /* out-projection + residual */
   PP_K_GATEUP,      /* gate/up projection + SiLU gating */
   PP_K_DOWN,        /* down-projection + residual */
   PP_K_TEXT_HEAD,   /* final norm, text head, greedy text token */
-  PP_K_DEP_INPROJ,  /* depformer: per-codebook input projection + token embedding */
+  PP_K_DEP_INPROJ,  /* depformer: input projections (tensor-core path: all codebooks in one
+                       launch, then each step's token embedding) */
   PP_K_DEP_NORM,    /* depformer: RMSNorms */
   PP_K_DEP_QKV,     /* depformer: QKV projection */
   PP_K_DEP_ATTN,    /* depformer: attention over the frame's steps */
