@@ -437,6 +437,7 @@ cudaError_t launch_attn(const Dims& D, const Buffers& b, int layer, bool op, con
   a.status = b.status;
   a.test_ctl = b.test_ctl;
   a.q_op = b.q_op;
+  a.early_trigger = D.B <= kEarlyTriggerMaxB;
   // the K/V maps span every layer's ring: slot coordinate = layer * B + slot
   return launch_attn_args(a, D.B, D.Dh, maps, layer * D.B, s);
 }

@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = ctl->tmem;
   pdl_wait_and_trigger();
+  if (a.early_trigger) pdl_trigger();
 
   auto next_valid = [&](int u) {
     while (u < u1 && decode_unit(a, u).nk == 0) ++u;

@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(128 * H, H == 1 ? 2 : 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
+  if (a.early_trigger) pdl_trigger();
 
   // rows of the weight boxes of this tile: the tile's kRows rows (boxes of 128 rows),
   // or its kPairs gate rows then the matching up rows (boxes of kPairs rows)

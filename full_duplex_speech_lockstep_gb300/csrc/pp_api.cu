@@ -449,6 +449,7 @@ cudaError_t mm_launch(const Dims& D, const Buffers& b, const Mm& g, int row0, in
   if (dec) a.dec = *dec;
   if (rope) a.rope = *rope;
   a.halves = g.H;
+  a.early_trigger = D.B <= kEarlyTriggerMaxB;
   a.chunks = ch.n;
   a.a_chunk_rows = ch.a_rows;
   a.b_chunk_rows = ch.b_rows;

@@ -85,7 +85,9 @@ typedef struct {
 /* Launch the tick's kernels without programmatic dependent launch.  By default each
  * kernel may start while its predecessor drains: a contraction allocates its tensor
  * memory and streams its first weight tiles (weights never depend on the previous
- * kernel), then waits for the predecessor before it reads any activation. */
+ * kernel), then waits for the predecessor before it reads any activation.  In engines
+ * of at most 8 slots a contraction or attention kernel releases its successor as soon as
+ * it starts, in larger ones after its main loop. */
 #define PP_FLAG_NO_PDL 0x2
 /* Split an engine of 16 or more slots into two groups that run as parallel branches of
  * the tick graph, so one group's latency-bound depformer can overlap the other's
