@@ -38,8 +38,8 @@ HBM_NOMINAL_GBS = 8000.0
 # dram__bytes_write of that launch per (slot, valid position).  Traffic grows in
 # proportion to the slots, so a full launch's traffic is this times slots x positions.
 # Valid only while k_attn_tc.cu is the source that was captured (its hash below).
-ATTN_TRAFFIC = {"bytes_per_slot_position": (1574.804e6 + 5.547776e6) / (32 * 3000),
-                "source_sha256_16": "d9b5f27b9abb31ed"}
+ATTN_TRAFFIC = {"bytes_per_slot_position": (1574.919e6 + 5.621248e6) / (32 * 3000),
+                "source_sha256_16": "dac474ff910b713b"}
 
 
 def parse():
