@@ -388,6 +388,7 @@ template <int E>  // head dim / 32
 __global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E))
 k_dep_attn(Dims D, Buffers b, int step, int layer, bool op) {
   pdl_wait_and_trigger();
+  pdl_trigger();   // small kernel: the next contraction may set up and prefetch meanwhile
   const int s = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
   float* out = b.dout + (size_t)s * D.dd + h * D.Dhd;
@@ -479,6 +480,7 @@ template <int E>  // head dim / 32
 __global__ void __launch_bounds__(kDepAttnMaxThreads(32 * E))
 k_dep_attn_b(Dims D, Buffers b, int layer) {
   pdl_wait_and_trigger();
+  pdl_trigger();   // small kernel: the next contraction may set up and prefetch meanwhile
   const int s = blockIdx.x, c = blockIdx.y, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (h >= D.Hd) return;
   const int k0 = D.nq - kDepBatch, step = k0 + c;
@@ -573,6 +575,7 @@ __global__ void __launch_bounds__(256) k_dep_in(Dims D, Buffers b, int k0, const
                                                 long long op_chunk, float* ssq) {
   __shared__ float sh[9];
   pdl_wait_and_trigger();
+  pdl_trigger();   // small kernel: the next contraction may set up and prefetch meanwhile
   const int s = blockIdx.x, c = blockIdx.y, k = k0 + c;
   const int t = tok[(size_t)c * D.B + s];
   const float* pz = b.pz + (size_t)s * D.nq * D.dd + (size_t)k * D.dd;
